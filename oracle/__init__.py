@@ -1,0 +1,41 @@
+"""Float64 CPU oracle for the streaming chunk-attention path.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it. It shares no code with the CUDA library (no kernels,
+headers, tables or constant generators); both receive the same seeded bf16
+inputs from the separate ``synthetic`` module.
+
+What it computes, and where the pages define it. The pages are
+  [H3-page]  "Interactive Coding Worlds with Real-time Streaming Diffusion
+             Render" (NVlabs Sol-Engine, StreamRender-H3 project page), and
+  [teardown] "StreamRender-H3: the engine paints flat colours, a 33B video
+             model paints the rest".
+
+* ``attention``  softmax(scale * Q K^T) V over the visible set with no mask:
+  attention inside the window is bidirectional ([H3-page] section 3.1.2), the
+  moving rows attend to the entire window ([H3-page] 3.1.2 "Prefix cache").
+* ``rope``       3D (t, h, w) rotary positions applied once, at the absolute
+  latent-frame index of the stream ([H3-page] 3.2 Iteration 3 item 2 and
+  Iteration 4).
+* ``ring``       preallocated ring of W frames written in place, oldest
+  evicted ([H3-page] 3.2 Iteration 3 item 2; 3.3 "Persistent KV layout").
+* ``session``    one static sink bank per denoising step ([H3-page] 3.3
+  "Static-context KV caching"; [teardown] "A window that slides, and a prefix
+  that doesn't"), two steps then commit.
+
+Every function here is pinned by ``tests/test_oracle_*.py`` against closed
+forms, invariants, library routines or brute force; no function is
+"parity unpinned".
+"""
+from .bf16 import bf16_bits_to_f64, f64_to_bf16_bits, round_bf16
+from .rope import axis_split, inverse_frequencies, token_positions, rope3d
+from .attention import attention, attention_rows
+from .ring import RingCache
+from .session import OracleSession
+
+__all__ = [
+    "bf16_bits_to_f64", "f64_to_bf16_bits", "round_bf16",
+    "axis_split", "inverse_frequencies", "token_positions", "rope3d",
+    "attention", "attention_rows", "RingCache", "OracleSession",
+]

@@ -1,0 +1,155 @@
+"""Pins for the oracle's ring cache and session (CPU only).
+
+Ring: the slot of frame g is g mod W, checked against a closed form for the
+slot table and against a deque brute force of "the last W frames".
+Session: the visible-set size of the H3 project page's worked example
+(tests/golden/decoder_window_visible_set.txt), causality (frames already
+evicted and future chunks change nothing), and clock-shift invariance of
+the scores (the Iteration 4 fix: scores depend only on time differences).
+"""
+import collections
+import math
+import os
+
+import numpy as np
+import pytest
+
+import synthetic as syn
+from oracle import (OracleSession, RingCache, attention, bf16_bits_to_f64, rope3d,
+                    token_positions)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = int(v)
+    return vals
+
+
+@pytest.mark.parametrize("W,F", [(4, 2), (6, 2), (5, 2), (3, 1), (8, 2)])
+def test_slot_table_closed_form_and_deque(W, F):
+    T, H, d = 3, 1, 2
+    ring = RingCache(W, T, H, d)
+    window = collections.deque(maxlen=W)
+    for chunk in range(23):
+        frames = np.arange(ring.n, ring.n + F, dtype=np.float64)
+        k = np.repeat(frames, T)[:, None, None] * np.ones((1, H, d))
+        ring.commit(k, -k, F)
+        window.extend(range(ring.n - F, ring.n))
+        n = ring.n
+        for s in range(W):
+            cands = [g for g in range(n) if g % W == s]
+            assert ring.slot_frame[s] == (max(cands) if cands else -1)
+            if cands:   # the slot holds exactly that frame's tokens
+                assert np.all(ring.k[s * T:(s + 1) * T] == max(cands))
+        assert sorted(g for g in ring.slot_frame if g >= 0) == sorted(window)
+        assert ring.slot_of(n) == n % W
+
+
+def test_visible_set_size_matches_pages_worked_example():
+    g = _load_golden("decoder_window_visible_set.txt")
+    sess = OracleSession(1, 8, g["grid_h"], g["grid_w"], g["chunk_frames"],
+                         g["window_frames"], g["n_sink"], 1)
+    Lq = sess.F * sess.T
+    assert Lq == g["queries"]
+    kz = np.zeros((Lq, 1, 8), np.uint16)
+    k, _ = sess.visible_kv(0, kz, kz)
+    assert k.shape[0] == g["keys_empty_cache"]
+    for _ in range(3):
+        sess.cache_commit(kz, kz)
+    k, _ = sess.visible_kv(0, kz, kz)
+    assert k.shape[0] == g["keys_full_cache"]
+
+
+def _session(shape, **kw):
+    sk, sv = syn.session_sinks(shape, 1)
+    return OracleSession(shape.n_heads, shape.head_dim, shape.grid_h, shape.grid_w,
+                         shape.chunk_frames, shape.window_frames, shape.n_sink,
+                         shape.n_steps, sk, sv, **kw)
+
+
+def test_evicted_frames_do_not_matter():
+    shape = syn.TINY
+    a, b = _session(shape), _session(shape)
+    for c in range(4):
+        x = syn.chunk_inputs(shape, 1, chunk=c)
+        a.cache_commit(x.clean_k, x.clean_v)
+        y = syn.chunk_inputs(shape, 1, chunk=c + 100) if c == 0 else x   # chunk 0 differs
+        b.cache_commit(y.clean_k, y.clean_v)
+    # W = 4 frames, F = 2: after 4 chunks frames 0 and 1 (chunk 0) are evicted
+    assert a.ring.n == 8 and sorted(a.ring.slot_frame) == [4, 5, 6, 7]
+    x = syn.chunk_inputs(shape, 1, chunk=9)
+    qa, ka = a.rope3d_qk(x.q[0], x.k[0])
+    qb, kb = b.rope3d_qk(x.q[0], x.k[0])
+    oa, la = a.chunk_attention(0, qa, ka, x.v[0])
+    ob, lb = b.chunk_attention(0, qb, kb, x.v[0])
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def test_uncommitted_future_chunk_does_not_leak():
+    shape = syn.TINY
+    a = _session(shape)
+    x = syn.chunk_inputs(shape, 1, chunk=0)
+    q, k = a.rope3d_qk(x.q[1], x.k[1])
+    before, _ = a.chunk_attention(1, q, k, x.v[1])
+    future = syn.chunk_inputs(shape, 1, chunk=1)
+    _ = a.rope3d_qk(future.q[0], future.k[0])    # rotating another chunk's Q/K is stateless
+    after, _ = a.chunk_attention(1, q, k, x.v[1])
+    assert np.array_equal(before, after)
+
+
+def test_step_selects_its_own_sink_bank():
+    shape = syn.TINY
+    a = _session(shape)
+    x = syn.chunk_inputs(shape, 1)
+    q, k = a.rope3d_qk(x.q[0], x.k[0])
+    o0, _ = a.chunk_attention(0, q, k, x.v[0])
+    o1, _ = a.chunk_attention(1, q, k, x.v[0])
+    assert not np.allclose(o0, o1)
+    kv = a.visible_kv(1, k, x.v[0])[0]
+    assert np.array_equal(kv[:shape.n_sink], a.sink_k[1])
+
+
+def test_clock_shift_invariance_without_sinks():
+    # With no unrotated sink keys in the visible set, every score depends only
+    # on time differences, so shifting the stream clock changes nothing
+    # (exactly, before bf16 rounding).
+    g = np.random.default_rng(0)
+    T, F, W, H, d = 6, 2, 4, 2, 64
+    hist = g.standard_normal((W * T, H, d))
+    chunk_k = g.standard_normal((F * T, H, d))
+    chunk_v = g.standard_normal((F * T, H, d))
+    q = g.standard_normal((F * T, H, d))
+    hist_v = g.standard_normal((W * T, H, d))
+    outs = []
+    for clock in (0, 100, 1000):
+        th, hh, wh = token_positions(W * T, 2, 3, clock)          # frames clock .. clock+3
+        tc, hc, wc = token_positions(F * T, 2, 3, clock + W)      # the chunk follows them
+        k = np.concatenate([rope3d(hist, th, hh, wh, 1e4), rope3d(chunk_k, tc, hc, wc, 1e4)])
+        v = np.concatenate([hist_v, chunk_v])
+        o, _ = attention(rope3d(q, tc, hc, wc, 1e4), k, v, 1 / 8)
+        outs.append(o)
+    assert np.allclose(outs[0], outs[1], rtol=0, atol=1e-11)
+    assert np.allclose(outs[0], outs[2], rtol=0, atol=1e-11)
+
+
+def test_commit_rotates_keys_at_absolute_frames():
+    shape = syn.TINY
+    a = _session(shape, t_clock0=50)
+    x0 = syn.chunk_inputs(shape, 1, chunk=0)
+    x1 = syn.chunk_inputs(shape, 1, chunk=1)
+    a.cache_commit(x0.clean_k, x0.clean_v)
+    a.cache_commit(x1.clean_k, x1.clean_v)
+    T = shape.tokens_per_frame
+    # frame 3 (second frame of chunk 1) is in slot 3 with time position 50 + 3
+    t, h, w = token_positions(T, shape.grid_h, shape.grid_w, 53)
+    want = rope3d(bf16_bits_to_f64(x1.clean_k)[T:2 * T], t, h, w, 1e4)
+    got = a.ring.k[3 * T:4 * T]
+    assert np.allclose(got, want, rtol=2.0 ** -8, atol=1e-30)
+    assert np.array_equal(a.ring.v[3 * T:4 * T], bf16_bits_to_f64(x1.clean_v)[T:2 * T])
