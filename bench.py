@@ -1,0 +1,385 @@
+"""Benchmark of the streaming chunk-attention hot path on GB300.
+
+One bench step = one streaming chunk of the 832x480 workload in steady state
+(ring full): for each of the two denoising steps, RoPE-3D on the chunk's Q/K
+and the chunk attention over sink bank + 6-frame ring + chunk; then the ring
+commit. Inputs are seeded synthetic bf16 N(0,1), resident in HBM before the
+timed region. Two independent sessions (about 280 MB of buffers each) are
+used alternately, so every step reads inputs that were last touched more
+than an L2's worth of traffic ago.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2|3]
+
+Multi-GPU: the path has no exchange step, so N ranks run N independent
+replicas (weak scaling, no collective on the data path); rank 0 prints the
+aggregate. ``--impl reference`` times the float64 CPU oracle on the host
+cores on a bounded sample of the same workload (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+import synthetic as syn
+
+METRIC = "chunk-attention ms/step and TFLOP/s on 1 GB300; % of bf16 tensor peak"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _make_session(shape, config, sess_id, dev):
+    import chunked_kv_cache_gb300 as sr
+    W = shape.window_frames
+    sink = lambda tid: syn.device_normal_bf16((shape.n_steps, shape.n_sink, shape.n_heads, shape.head_dim), dev,
+                                              config, sess_id, 0, 0, tid)
+    s = sr.Session(shape.n_heads, shape.head_dim, shape.grid_h, shape.grid_w, shape.chunk_frames, W,
+                   shape.n_sink, shape.n_steps, sink_k=sink(syn.T_SINK_K), sink_v=sink(syn.T_SINK_V), device=dev)
+    s.ring_k.copy_(syn.device_normal_bf16(tuple(s.ring_k.shape), dev, config, sess_id, 0, 0, syn.T_RING_K))
+    s.ring_v.copy_(syn.device_normal_bf16(tuple(s.ring_v.shape), dev, config, sess_id, 0, 0, syn.T_RING_V))
+    s.slot_frame.copy_(torch.arange(W, dtype=torch.int32, device=dev))
+    s.restore(W)                                   # steady state: ring full
+    x = syn.chunk_inputs_device(shape, config, dev, session=sess_id, chunk=0)
+    x["o"] = [torch.empty_like(x["q"][0]) for _ in range(shape.n_steps)]
+    return s, x
+
+
+def _chunk(s, x, n_steps, ev=None):
+    """One streaming chunk through the library: 2 x (RoPE + attention) + commit."""
+    for st in range(n_steps):
+        if ev is not None:
+            ev["rope"][0].record()
+        s.rope3d_qk(x["q"][st], x["k"][st])
+        if ev is not None:
+            ev["rope"][1].record()
+            ev["attn"][0].record()
+        s.chunk_attention(st, x["q"][st], x["k"][st], x["v"][st], out=x["o"][st])
+        if ev is not None:
+            ev["attn"][1].record()
+    if ev is not None:
+        ev["commit"][0].record()
+    s.cache_commit(x["clean_k"], x["clean_v"])
+    if ev is not None:
+        ev["commit"][1].record()
+
+
+def run_ours(args):
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_kv_cache_gb300 import build
+    build.build()
+    shape = syn.SHAPES[args.config]
+    full = shape.window_frames
+    flops_attn = shape.attention_flops(full)               # one denoising step
+    flops_chunk = shape.n_steps * flops_attn
+    commit_bytes = 4 * shape.lq * shape.n_heads * shape.head_dim * 2
+    sessions = [_make_session(shape, args.config, i + 10 * rank, dev) for i in range(2)]
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        s, x = sessions[i % 2]
+        _chunk(s, x, shape.n_steps)
+    torch.cuda.synchronize()
+
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [{"rope": None, "attn": None, "commit": None} for _ in range(args.steps)]
+    per = []
+    for e in evs:
+        per.append({k: [mk() for _ in range(shape.n_steps)] if k != "commit" else [mk()] for k in e})
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        t0.record()
+        for i in range(args.steps):
+            s, x = sessions[i % 2]
+            p = per[i]
+            for st in range(shape.n_steps):
+                p["rope"][st][0].record()
+                s.rope3d_qk(x["q"][st], x["k"][st])
+                p["rope"][st][1].record()
+                p["attn"][st][0].record()
+                s.chunk_attention(st, x["q"][st], x["k"][st], x["v"][st], out=x["o"][st])
+                p["attn"][st][1].record()
+            p["commit"][0][0].record()
+            s.cache_commit(x["clean_k"], x["clean_v"])
+            p["commit"][0][1].record()
+        t1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    attn_ms = [a[0].elapsed_time(a[1]) for p in per for a in p["attn"]]
+    rope_ms = [a[0].elapsed_time(a[1]) for p in per for a in p["rope"]]
+    commit_ms = [a[0].elapsed_time(a[1]) for p in per for a in p["commit"]]
+    for s, _ in sessions:
+        if s.error_status() != 0:
+            raise RuntimeError("device error word set during the bench")
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    # end to end through the public API: pinned host inputs in, result out
+    e2e = run_e2e(shape, args, dev, sessions[0][0]) if not args.profile else {"seconds": 1.0, "chunks": 0,
+                                                                              "h2d": 0, "d2h": 0}
+    if world > 1:
+        t = torch.tensor([e2e["seconds"]], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e["seconds"] = float(t.item())
+    clocks = clk.summary()
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak_tf, peak_gbs, peak_kind = _peaks()
+    attn_avg = statistics.mean(attn_ms)
+    achieved = flops_attn / (attn_avg / 1e3) / 1e12
+    value = world * args.steps * flops_chunk / elapsed / 1e12
+    commit_avg = statistics.mean(commit_ms)
+    rope_avg = statistics.mean(rope_ms)
+    cpu = cpu_baseline(shape, args) if world == 1 and not args.profile else None
+    traffic = _profiled_traffic("chunk_attention", args.config)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": shape.name + ", steady state (ring full), one step = one chunk: "
+                               "2 x (RoPE-3D + chunk attention) + ring commit",
+                   "heads": shape.n_heads, "head_dim": shape.head_dim, "lq": shape.lq,
+                   "lk": shape.lk(full), "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: two ~280 MB sessions used alternately"},
+        "attention_ms_per_denoise_step": round(attn_avg, 4),
+        "attention_tflops": round(achieved, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4), "traffic": traffic,
+                     "kernel": "attn_kernel (sr_chunk_attention)",
+                     "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "kernels": {
+            "commit": {"us": round(commit_avg * 1e3, 2), "GB/s": round(commit_bytes / (commit_avg / 1e3) / 1e9, 1),
+                       "frac_hbm": round(commit_bytes / (commit_avg / 1e3) / 1e9 / peak_gbs, 4)},
+            "rope3d_qk": {"us": round(rope_avg * 1e3, 2),
+                          "GB/s": round(commit_bytes / (rope_avg / 1e3) / 1e9, 1),
+                          "frac_hbm": round(commit_bytes / (rope_avg / 1e3) / 1e9 / peak_gbs, 4)},
+        },
+        "e2e": {"value": round(world * e2e["chunks"] * flops_chunk / e2e["seconds"] / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": (2 * shape.n_steps + 1) * args.steps,
+    }
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(shape, args, dev, sess):
+    """Same chunk through the public API with the step's inputs copied in from
+    pinned host memory and both steps' outputs copied back, every step."""
+    n = max(3, min(args.steps, 10))
+    dims = (shape.lq, shape.n_heads, shape.head_dim)
+    g = torch.Generator().manual_seed(1234)
+    host_in = [torch.randn(dims, generator=g).to(torch.bfloat16).pin_memory()
+               for _ in range(3 * shape.n_steps + 2)]
+    host_out = [torch.empty(dims, dtype=torch.bfloat16).pin_memory() for _ in range(shape.n_steps)]
+    dev_in = [torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in host_in]
+    dev_out = [torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in host_out]
+
+    def one():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        for st in range(shape.n_steps):
+            q, k, v = dev_in[3 * st], dev_in[3 * st + 1], dev_in[3 * st + 2]
+            sess.rope3d_qk(q, k)
+            sess.chunk_attention(st, q, k, v, out=dev_out[st])
+        sess.cache_commit(dev_in[-2], dev_in[-1])
+        for d, h in zip(dev_out, host_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(n):
+        one()
+    torch.cuda.synchronize()
+    sec = time.perf_counter() - t
+    per = dims[0] * dims[1] * dims[2] * 2
+    return {"seconds": sec, "chunks": n, "h2d": per * len(host_in), "d2h": per * len(host_out)}
+
+
+def _profiled_traffic(kernel, config):
+    """DRAM bytes per launch from the committed ncu summary, if it matches."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}/config{config}")
+    return None if e is None or e.get("stale") else e.get("bytes_per_launch")
+
+
+def cpu_baseline(shape, args, budget_s: float = 12.0):
+    """The float64 oracle, as it stands, on this host's cores: attention of
+    whole heads of one denoising step (full window) until the time budget is
+    used; returns TFLOP/s scaled by the sampled fraction."""
+    from oracle import attention, bf16_bits_to_f64
+    full = shape.window_frames
+    lk = shape.lk(full)
+    g = np.random.default_rng(0)
+    heads_done, t_used = 0, 0.0
+    while t_used < budget_s and heads_done < shape.n_heads:
+        q = g.standard_normal((shape.lq, 1, shape.head_dim))
+        k = g.standard_normal((lk, 1, shape.head_dim))
+        v = g.standard_normal((lk, 1, shape.head_dim))
+        t = time.perf_counter()
+        attention(q, k, v, 1.0 / math.sqrt(shape.head_dim))
+        t_used += time.perf_counter() - t
+        heads_done += 1
+    flops = 4.0 * heads_done * shape.lq * lk * shape.head_dim
+    return {"value": round(flops / t_used / 1e12, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{heads_done} of {shape.n_heads} heads of one denoising step "
+                      f"({shape.lq} queries x {lk} keys, float64 numpy), {t_used:.1f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the float64 oracle on the host cores, each step a bounded
+    sample (one head of one denoising step, full window) of the same workload."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    from oracle import OracleSession, attention
+    shape = syn.SHAPES[args.config]
+    full = shape.window_frames
+    lk = shape.lk(full)
+    g = np.random.default_rng(0)
+    q = g.standard_normal((shape.lq, 1, shape.head_dim))
+    k = g.standard_normal((lk, 1, shape.head_dim))
+    v = g.standard_normal((lk, 1, shape.head_dim))
+    scale = 1.0 / math.sqrt(shape.head_dim)
+    for _ in range(args.warmup):
+        attention(q, k, v, scale)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        attention(q, k, v, scale)
+    sec = time.perf_counter() - t
+    flops = 4.0 * shape.lq * lk * shape.head_dim
+    value = args.steps * flops / sec / 1e12
+    sample = f"one head of one denoising step per bench step ({shape.lq} queries x {lk} keys, float64 numpy)"
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": shape.name + ", steady state (ring full)", "heads": shape.n_heads,
+                      "lq": shape.lq, "lk": lk},
+           "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, choices=[2, 3], default=2)
+    ap.add_argument("--profile", action="store_true",
+                    help="under a profiler: skip the end-to-end and CPU-baseline legs (their numbers are not reported)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

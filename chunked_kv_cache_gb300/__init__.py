@@ -1,0 +1,162 @@
+"""GB300-native streaming chunk attention with a 3D-RoPE ring-buffer KV cache.
+
+The compute lives in libsr.so (hand-written CUDA for sm_103a, C ABI in
+include/sr.h). This package is the thin Python side: the ctypes binding with
+the C names (``_native``) and ``Session``, which allocates a session's
+persistent device buffers with torch and marshals tensors into those calls.
+torch provides device memory and streams only; nothing here computes.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import (SrConfig, SrBuffers, SrError, sr_session_init, sr_session_restore, sr_session_frames,
+                      sr_rope3d_qk, sr_chunk_attention, sr_cache_commit, sr_session_free,
+                      sr_chunk_attention_batch, sr_device_error_status, sr_debug_wait_timeout,
+                      SR_MAX_BATCH)
+
+__all__ = [
+    "Session", "chunk_attention_batch", "SrConfig", "SrBuffers", "SrError",
+    "sr_session_init", "sr_session_restore", "sr_session_frames", "sr_rope3d_qk", "sr_chunk_attention",
+    "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch", "sr_device_error_status",
+    "sr_debug_wait_timeout",
+]
+
+_BF16 = torch.bfloat16
+
+
+def _ptr(t: torch.Tensor | None) -> int:
+    return 0 if t is None or t.numel() == 0 else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_tensor(name: str, t: torch.Tensor, shape, device, dtype=_BF16) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or t.device != device:
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device} (contiguous={t.is_contiguous()})")
+
+
+class Session:
+    """One streaming session and its caller-owned device buffers.
+
+    Buffers: per-step sink banks [n_steps][S][H][d], ring K/V [W*T][H][d],
+    slot table [W] int32 and an error word, all bf16 unless stated, all
+    allocated here with torch and handed to the library by pointer.
+    """
+
+    def __init__(self, n_heads: int, head_dim: int, grid_h: int, grid_w: int, chunk_frames: int,
+                 window_frames: int, n_sink: int, n_steps: int = 2, *, sink_k: torch.Tensor | None = None,
+                 sink_v: torch.Tensor | None = None, t_clock0: int = 0, rope_base: float = 10000.0,
+                 softmax_scale: float = 0.0, wait_timeout_ns: int = 0, device="cuda"):
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.H, self.d = n_heads, head_dim
+        self.T = grid_h * grid_w
+        self.F, self.W, self.S, self.n_steps = chunk_frames, window_frames, n_sink, n_steps
+        self.lq = chunk_frames * self.T
+        dev = self.device
+        self.sink_k = torch.empty((n_steps, n_sink, n_heads, head_dim), dtype=_BF16, device=dev)
+        self.sink_v = torch.empty_like(self.sink_k)
+        self.ring_k = torch.empty((window_frames * self.T, n_heads, head_dim), dtype=_BF16, device=dev)
+        self.ring_v = torch.empty_like(self.ring_k)
+        self.slot_frame = torch.empty((max(window_frames, 1),), dtype=torch.int32, device=dev)
+        self.err_word = torch.zeros((1,), dtype=torch.int32, device=dev)
+        if (sink_k is None) != (sink_v is None):
+            raise ValueError("give both sink_k and sink_v, or neither")
+        if sink_k is not None:
+            _check_tensor("sink_k", sink_k, self.sink_k.shape, dev)
+            _check_tensor("sink_v", sink_v, self.sink_v.shape, dev)
+        self.cfg = SrConfig(n_heads, head_dim, grid_h, grid_w, chunk_frames, window_frames, n_sink, n_steps,
+                            t_clock0, rope_base, softmax_scale, wait_timeout_ns)
+        self.bufs = SrBuffers(_ptr(self.sink_k), _ptr(self.sink_v), _ptr(self.ring_k), _ptr(self.ring_v),
+                              self.slot_frame.data_ptr(), self.err_word.data_ptr())
+        self.handle = None
+        with torch.cuda.device(dev):
+            self.handle = sr_session_init(self.cfg, self.bufs, _ptr(sink_k), _ptr(sink_v), _stream(dev))
+
+    # ---------------------------------------------------------------- state
+    @property
+    def frames(self) -> int:
+        return sr_session_frames(self.handle)
+
+    def restore(self, n_committed: int) -> None:
+        sr_session_restore(self.handle, n_committed)
+
+    def error_status(self) -> int:
+        """Synchronises the stream and maps the device error word to a status."""
+        return sr_device_error_status(int(self.err_word.item()))
+
+    def _chunk(self, name: str, t: torch.Tensor) -> None:
+        _check_tensor(name, t, (self.lq, self.H, self.d), self.device)
+
+    # ---------------------------------------------------------------- calls
+    def rope3d_qk(self, q: torch.Tensor | None, k: torch.Tensor | None) -> None:
+        for name, t in (("q", q), ("k", k)):
+            if t is not None:
+                self._chunk(name, t)
+        sr_rope3d_qk(self.handle, _ptr(q), _ptr(k), _stream(self.device))
+
+    def chunk_attention(self, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = None):
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            self._chunk(name, t)
+        if out is None:
+            out = torch.empty_like(q)
+        self._chunk("out", out)
+        if lse is True:
+            lse = torch.empty((self.H, self.lq), dtype=torch.float32, device=self.device)
+        if isinstance(lse, torch.Tensor):
+            _check_tensor("lse", lse, (self.H, self.lq), self.device, torch.float32)
+        else:
+            lse = None
+        sr_chunk_attention(self.handle, step, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           _ptr(lse), _stream(self.device))
+        return (out, lse) if lse is not None else out
+
+    def cache_commit(self, k: torch.Tensor, v: torch.Tensor) -> None:
+        self._chunk("k", k)
+        self._chunk("v", v)
+        sr_cache_commit(self.handle, k.data_ptr(), v.data_ptr(), _stream(self.device))
+
+    def close(self) -> None:
+        if self.handle is not None:
+            sr_session_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def chunk_attention_batch(sessions, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                          out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = None):
+    """One launch over several sessions' chunks packed along L (session i owns
+    rows [off[i], off[i+1]) with off the running sum of each session's F*T)."""
+    s0 = sessions[0]
+    offs = [0]
+    for s in sessions:
+        offs.append(offs[-1] + s.lq)
+    shape = (offs[-1], s0.H, s0.d)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, shape, s0.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor("out", out, shape, s0.device)
+    if lse is True:
+        lse = torch.empty((s0.H, offs[-1]), dtype=torch.float32, device=s0.device)
+    if isinstance(lse, torch.Tensor):
+        _check_tensor("lse", lse, (s0.H, offs[-1]), s0.device, torch.float32)
+    else:
+        lse = None
+    sr_chunk_attention_batch([s.handle for s in sessions], step, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                             offs, out.data_ptr(), _ptr(lse), _stream(s0.device))
+    return (out, lse) if lse is not None else out

@@ -1,0 +1,148 @@
+"""ctypes binding of libsr.so: the C ABI of include/sr.h, argument marshalling only.
+
+Every function keeps the C name and takes plain integers for device pointers
+and for the CUDA stream. No computation happens here; if the library is
+missing, loading raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsr.so")
+
+SR_OK = 0
+SR_ERR_INVALID_ARG = -1
+SR_ERR_UNSUPPORTED = -2
+SR_ERR_ALIGN = -3
+SR_ERR_STATE = -4
+SR_ERR_CUDA = -5
+SR_ERR_TIMEOUT = -6
+SR_DEVERR_WAIT_TIMEOUT = 1
+SR_MAX_BATCH = 16
+
+# every extern "C" symbol that include/sr.h declares
+EXPORTS = (
+    "sr_session_init", "sr_session_restore", "sr_session_frames", "sr_rope3d_qk",
+    "sr_chunk_attention", "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch",
+    "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string",
+)
+
+
+class SrConfig(ctypes.Structure):
+    _fields_ = [
+        ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("grid_h", ctypes.c_int32), ("grid_w", ctypes.c_int32),
+        ("chunk_frames", ctypes.c_int32), ("window_frames", ctypes.c_int32),
+        ("n_sink", ctypes.c_int32), ("n_steps", ctypes.c_int32),
+        ("t_clock0", ctypes.c_int32), ("rope_base", ctypes.c_float),
+        ("softmax_scale", ctypes.c_float), ("wait_timeout_ns", ctypes.c_uint64),
+    ]
+
+
+class SrBuffers(ctypes.Structure):
+    _fields_ = [
+        ("sink_k", ctypes.c_void_p), ("sink_v", ctypes.c_void_p),
+        ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p),
+        ("slot_frame", ctypes.c_void_p), ("err_word", ctypes.c_void_p),
+    ]
+
+
+class SrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsr.so once (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: build it with `python -m chunked_kv_cache_gb300.build` "
+                          "(there is no fallback implementation)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+        L.sr_session_init.argtypes = [ctypes.POINTER(SrConfig), ctypes.POINTER(SrBuffers), vp, vp, vp,
+                                      ctypes.POINTER(vp)]
+        L.sr_session_restore.argtypes = [vp, i64]
+        L.sr_session_frames.argtypes = [vp, ctypes.POINTER(i64)]
+        L.sr_rope3d_qk.argtypes = [vp, vp, vp, vp]
+        L.sr_chunk_attention.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+        L.sr_cache_commit.argtypes = [vp, vp, vp, vp]
+        L.sr_session_free.argtypes = [vp]
+        L.sr_chunk_attention_batch.argtypes = [ctypes.POINTER(vp), i32, i32, vp, vp, vp,
+                                               ctypes.POINTER(i64), vp, vp, vp]
+        L.sr_device_error_status.argtypes = [i32]
+        L.sr_debug_wait_timeout.argtypes = [vp, u64, vp]
+        L.sr_status_string.argtypes = [ctypes.c_int]
+        L.sr_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name != "sr_status_string":
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return lib().sr_status_string(int(st)).decode()
+
+
+def _check(st: int, what: str) -> None:
+    if st != SR_OK:
+        raise SrError(st, what)
+
+
+def sr_session_init(cfg: SrConfig, bufs: SrBuffers, sink_k_src: int, sink_v_src: int, stream: int) -> int:
+    out = ctypes.c_void_p()
+    _check(lib().sr_session_init(ctypes.byref(cfg), ctypes.byref(bufs), sink_k_src or None,
+                                 sink_v_src or None, stream or None, ctypes.byref(out)), "sr_session_init")
+    return out.value
+
+
+def sr_session_restore(handle: int, n_committed: int) -> None:
+    _check(lib().sr_session_restore(handle, int(n_committed)), "sr_session_restore")
+
+
+def sr_session_frames(handle: int) -> int:
+    n = ctypes.c_int64()
+    _check(lib().sr_session_frames(handle, ctypes.byref(n)), "sr_session_frames")
+    return n.value
+
+
+def sr_rope3d_qk(handle: int, q: int, k: int, stream: int) -> None:
+    _check(lib().sr_rope3d_qk(handle, q or None, k or None, stream or None), "sr_rope3d_qk")
+
+
+def sr_chunk_attention(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int, stream: int) -> None:
+    _check(lib().sr_chunk_attention(handle, int(step), q, k, v, o, lse or None, stream or None),
+           "sr_chunk_attention")
+
+
+def sr_cache_commit(handle: int, k_raw: int, v: int, stream: int) -> None:
+    _check(lib().sr_cache_commit(handle, k_raw, v, stream or None), "sr_cache_commit")
+
+
+def sr_session_free(handle: int) -> None:
+    _check(lib().sr_session_free(handle), "sr_session_free")
+
+
+def sr_chunk_attention_batch(handles, step: int, q: int, k: int, v: int, q_off, o: int, lse: int,
+                             stream: int) -> None:
+    n = len(handles)
+    arr = (ctypes.c_void_p * n)(*handles)
+    offs = (ctypes.c_int64 * (n + 1))(*[int(x) for x in q_off])
+    _check(lib().sr_chunk_attention_batch(arr, n, int(step), q, k, v, offs, o, lse or None, stream or None),
+           "sr_chunk_attention_batch")
+
+
+def sr_device_error_status(value: int) -> int:
+    return lib().sr_device_error_status(int(value))
+
+
+def sr_debug_wait_timeout(err_word: int, timeout_ns: int, stream: int) -> None:
+    _check(lib().sr_debug_wait_timeout(err_word, int(timeout_ns), stream or None), "sr_debug_wait_timeout")

@@ -1,0 +1,403 @@
+// sr_api.cu -- the C ABI of libsr.so (declared in include/sr.h): argument
+// validation, the per-session state machine, tensor-map encoding and launches.
+//
+// Host state per session mirrors the streaming loop of the H3 project page
+// ("Interactive Coding Worlds with Real-time Streaming Diffusion Render"):
+// static-context banks written once (section 3.3 "Static-context KV caching"),
+// a preallocated ring of W frames updated in place (section 3.2 Iteration 3
+// item 2; 3.3 "Persistent KV layout") and the number of frames committed so
+// far, which fixes both the rotary time of the chunk and the occupied ring
+// prefix. Everything an attention call needs is derived on the host from that
+// count, so no call waits on the device (section 3.3 "Attention metadata
+// reuse": no host-device synchronisation per call).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "sr.h"
+#include "sr_kernels.h"
+
+struct sr_session {
+  sr_config cfg;
+  sr_buffers buf;
+  int64_t tokens_per_frame;   // T
+  int64_t lq;                 // F*T
+  float scale;
+  int64_t n_committed;
+  double inv_freq[64];
+  int8_t axis[64];
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kBoxRows = 128;
+constexpr int kBoxCols = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sr_status validate_config(const sr_config& c) {
+  if (c.n_heads < 1 || c.grid_h < 1 || c.grid_w < 1 || c.chunk_frames < 1 || c.window_frames < 0 ||
+      c.n_sink < 0 || c.n_steps < 1)
+    return SR_ERR_INVALID_ARG;
+  if (c.head_dim != 64 && c.head_dim != 128) return SR_ERR_UNSUPPORTED;
+  if (c.window_frames > 0 && c.window_frames < c.chunk_frames) return SR_ERR_INVALID_ARG;
+  if (!(c.rope_base > 1.0f) || !std::isfinite(c.rope_base)) return SR_ERR_INVALID_ARG;
+  if (!std::isfinite(c.softmax_scale)) return SR_ERR_INVALID_ARG;
+  // every element offset must fit comfortably in 32-bit row counts
+  const int64_t row = static_cast<int64_t>(c.n_heads) * c.head_dim;
+  const int64_t T = static_cast<int64_t>(c.grid_h) * c.grid_w;
+  const int64_t lq = T * c.chunk_frames;
+  const int64_t ring_rows = T * c.window_frames;
+  const int64_t limit = int64_t(1) << 30;
+  if (row > 65536 || lq > limit / 4 || ring_rows > limit / 4 || c.n_sink > limit / 4 ||
+      lq * row > limit || ring_rows * row > limit || static_cast<int64_t>(c.n_sink) * row * c.n_steps > limit)
+    return SR_ERR_INVALID_ARG;
+  return SR_OK;
+}
+
+// Rotary tables: pair p of the head (dims 2p, 2p+1) belongs to axis t, h or w
+// and turns by position * base^(-2i/d_axis), i its index inside the axis. The
+// head dim splits into [d_t | d_h | d_w], d_h = d_w = 2*floor(d/6).
+void build_rope_tables(sr_session* s) {
+  const int d = s->cfg.head_dim;
+  const int dh = 2 * (d / 6);
+  const int dt = d - 2 * dh;
+  const int dims[3] = {dt, dh, dh};
+  int p = 0;
+  for (int a = 0; a < 3; ++a) {
+    for (int i = 0; i < dims[a] / 2; ++i, ++p) {
+      s->axis[p] = static_cast<int8_t>(a);
+      s->inv_freq[p] = std::pow(static_cast<double>(s->cfg.rope_base), -2.0 * i / static_cast<double>(dims[a]));
+    }
+  }
+  for (; p < 64; ++p) {
+    s->axis[p] = 0;
+    s->inv_freq[p] = 0.0;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D map over a token-major bf16 tensor [rows][row_elems], box {64, 128},
+// 128-byte swizzle, zero fill outside [0, rows).
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t row_elems) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * 2)};
+  cuuint32_t box[2] = {kBoxCols, kBoxRows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+// Max dynamic shared memory is a per-device function attribute: set it once
+// per device and template.
+cudaError_t ensure_attn_attr(int head_dim, int nsess_template) {
+  static std::mutex mu;
+  static bool done[64][2][2];
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int hi = head_dim == 128 ? 1 : 0, ni = nsess_template == 1 ? 0 : 1;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev][hi][ni]) return cudaSuccess;
+  cudaError_t e = sr::attn_prepare(head_dim, nsess_template);
+  if (e == cudaSuccess) done[dev][hi][ni] = true;
+  return e;
+}
+
+// Fill one session's segment maps for `step` (rows of the chunk taken from
+// k, v at row offset `row0` of a packed tensor).
+sr_status fill_session(sr::AttnSession& out, const sr_session* s, int step, const void* k, const void* v,
+                       int64_t row0) {
+  const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
+  const int64_t S = s->cfg.n_sink;
+  const int64_t W = s->cfg.window_frames;
+  const int64_t valid_frames = std::min<int64_t>(s->n_committed, W);
+  const int64_t ring_rows = valid_frames * s->tokens_per_frame;
+  std::memset(&out, 0, sizeof(out));
+  out.seg_rows[0] = static_cast<int32_t>(S);
+  out.seg_rows[1] = static_cast<int32_t>(ring_rows);
+  out.seg_rows[2] = static_cast<int32_t>(s->lq);
+  const size_t bank_off = static_cast<size_t>(step) * S * row_elems * 2;
+  if (S > 0) {
+    if (!encode_rows(&out.kmap[0], static_cast<const char*>(s->buf.sink_k) + bank_off, S, row_elems) ||
+        !encode_rows(&out.vmap[0], static_cast<const char*>(s->buf.sink_v) + bank_off, S, row_elems))
+      return SR_ERR_CUDA;
+  }
+  if (ring_rows > 0) {
+    if (!encode_rows(&out.kmap[1], s->buf.ring_k, ring_rows, row_elems) ||
+        !encode_rows(&out.vmap[1], s->buf.ring_v, ring_rows, row_elems))
+      return SR_ERR_CUDA;
+  }
+  const char* kc = static_cast<const char*>(k) + static_cast<size_t>(row0) * row_elems * 2;
+  const char* vc = static_cast<const char*>(v) + static_cast<size_t>(row0) * row_elems * 2;
+  if (!encode_rows(&out.kmap[2], kc, s->lq, row_elems) || !encode_rows(&out.vmap[2], vc, s->lq, row_elems))
+    return SR_ERR_CUDA;
+  out.q_row0 = static_cast<int32_t>(row0);
+  out.lq = static_cast<int32_t>(s->lq);
+  out.nqb = static_cast<int32_t>((s->lq + 255) / 256);
+  return SR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sr_status_string(sr_status st) {
+  switch (st) {
+    case SR_OK: return "ok";
+    case SR_ERR_INVALID_ARG: return "invalid argument";
+    case SR_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SR_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case SR_ERR_STATE: return "call not allowed in the session's state";
+    case SR_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case SR_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+sr_status sr_device_error_status(int32_t v) { return v == SR_DEVERR_NONE ? SR_OK : SR_ERR_TIMEOUT; }
+
+sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const void* sink_k_src,
+                          const void* sink_v_src, void* stream, sr_session** out) {
+  if (out) *out = nullptr;
+  if (!cfg || !bufs || !out) return SR_ERR_INVALID_ARG;
+  sr_status st = validate_config(*cfg);
+  if (st != SR_OK) return st;
+  const bool has_sink = cfg->n_sink > 0;
+  const bool has_ring = cfg->window_frames > 0;
+  if ((has_sink && (!bufs->sink_k || !bufs->sink_v)) || (has_ring && (!bufs->ring_k || !bufs->ring_v)) ||
+      (has_ring && !bufs->slot_frame) || !bufs->err_word)
+    return SR_ERR_INVALID_ARG;
+  if ((sink_k_src == nullptr) != (sink_v_src == nullptr)) return SR_ERR_INVALID_ARG;
+  if ((has_sink && (!aligned16(bufs->sink_k) || !aligned16(bufs->sink_v))) ||
+      (has_ring && (!aligned16(bufs->ring_k) || !aligned16(bufs->ring_v))) ||
+      (sink_k_src && (!aligned16(sink_k_src) || !aligned16(sink_v_src))) ||
+      (reinterpret_cast<uintptr_t>(bufs->err_word) & 3u) ||
+      (reinterpret_cast<uintptr_t>(bufs->slot_frame) & 3u))
+    return SR_ERR_ALIGN;
+
+  sr_session* s = new (std::nothrow) sr_session;
+  if (!s) return SR_ERR_INVALID_ARG;
+  std::memset(s, 0, sizeof(*s));
+  s->cfg = *cfg;
+  if (s->cfg.wait_timeout_ns == 0) s->cfg.wait_timeout_ns = kDefaultTimeoutNs;
+  s->buf = *bufs;
+  s->tokens_per_frame = static_cast<int64_t>(cfg->grid_h) * cfg->grid_w;
+  s->lq = s->tokens_per_frame * cfg->chunk_frames;
+  s->scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / std::sqrt(static_cast<float>(cfg->head_dim));
+  s->n_committed = 0;
+  build_rope_tables(s);
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (sink_k_src && has_sink) {
+    const size_t bytes = static_cast<size_t>(cfg->n_steps) * cfg->n_sink * cfg->n_heads * cfg->head_dim * 2;
+    e = sr::launch_copy16(bufs->sink_k, sink_k_src, bytes, cs);
+    if (e == cudaSuccess) e = sr::launch_copy16(bufs->sink_v, sink_v_src, bytes, cs);
+  }
+  if (e == cudaSuccess) e = sr::launch_init_ring_state(bufs->slot_frame, cfg->window_frames, bufs->err_word, cs);
+  if (e == cudaSuccess) e = ensure_attn_attr(cfg->head_dim, 1);
+  if (e == cudaSuccess) e = ensure_attn_attr(cfg->head_dim, sr::kAttnMaxBatch);
+  if (e != cudaSuccess) {
+    delete s;
+    return SR_ERR_CUDA;
+  }
+  *out = s;
+  return SR_OK;
+}
+
+sr_status sr_session_restore(sr_session* s, int64_t n_committed) {
+  if (!s || n_committed < 0 || n_committed > (int64_t(1) << 40)) return SR_ERR_INVALID_ARG;
+  s->n_committed = n_committed;
+  return SR_OK;
+}
+
+sr_status sr_session_frames(const sr_session* s, int64_t* n) {
+  if (!s || !n) return SR_ERR_INVALID_ARG;
+  *n = s->n_committed;
+  return SR_OK;
+}
+
+static sr_status rope_common(sr_session* s, const void* a_src, const void* b_src, void* a_dst, void* b_dst,
+                             int mode, void* stream) {
+  sr::RopeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.src0 = static_cast<const __nv_bfloat16*>(a_src);
+  p.src1 = static_cast<const __nv_bfloat16*>(b_src);
+  p.dst0 = static_cast<__nv_bfloat16*>(a_dst);
+  p.dst1 = static_cast<__nv_bfloat16*>(b_dst);
+  p.slot_frame = s->buf.slot_frame;
+  p.n_committed = s->n_committed;
+  p.n_tok = static_cast<int32_t>(s->lq);
+  p.n_heads = s->cfg.n_heads;
+  p.tokens_per_frame = static_cast<int32_t>(s->tokens_per_frame);
+  p.grid_w = s->cfg.grid_w;
+  p.window_frames = s->cfg.window_frames;
+  p.chunk_frames = s->cfg.chunk_frames;
+  p.t_clock0 = s->cfg.t_clock0;
+  p.mode = mode;
+  std::memcpy(p.inv_freq, s->inv_freq, sizeof(p.inv_freq));
+  std::memcpy(p.axis, s->axis, sizeof(p.axis));
+  cudaError_t e = sr::launch_rope(p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SR_OK : SR_ERR_CUDA;
+}
+
+sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream) {
+  if (!s) return SR_ERR_INVALID_ARG;
+  if ((q && !aligned16(q)) || (k && !aligned16(k))) return SR_ERR_ALIGN;
+  if (!q && !k) return SR_OK;
+  // a single tensor: rotate it twice over the same pointer is wrong, so pair
+  // it with itself only through the first operand and a scratch-free no-op
+  if (q && k) return rope_common(s, q, k, q, k, 0, stream);
+  // One tensor: pass it as both operands. Each 16-byte vector is loaded by one
+  // thread into two registers before either store, so both stores write the
+  // same once-rotated value.
+  void* x = q ? q : k;
+  return rope_common(s, x, x, x, x, 0, stream);
+}
+
+sr_status sr_cache_commit(sr_session* s, const void* k_raw, const void* v, void* stream) {
+  if (!s || !k_raw || !v) return SR_ERR_INVALID_ARG;
+  if (!aligned16(k_raw) || !aligned16(v)) return SR_ERR_ALIGN;
+  if (s->cfg.window_frames == 0) {
+    s->n_committed += s->cfg.chunk_frames;
+    return SR_OK;
+  }
+  sr_status st = rope_common(s, k_raw, v, s->buf.ring_k, s->buf.ring_v, 1, stream);
+  if (st == SR_OK) s->n_committed += s->cfg.chunk_frames;
+  return st;
+}
+
+sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const void* k, const void* v, void* o,
+                             float* lse, void* stream) {
+  if (!s || !q || !k || !v || !o) return SR_ERR_INVALID_ARG;
+  if (step < 0 || step >= s->cfg.n_steps) return SR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return SR_ERR_ALIGN;
+  auto* p = new (std::nothrow) sr::AttnParams<1>;
+  if (!p) return SR_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
+  sr_status st = SR_OK;
+  if (!encode_rows(&p->qmap, q, s->lq, row_elems)) st = SR_ERR_CUDA;
+  if (st == SR_OK) st = fill_session(p->sess[0], s, step, k, v, 0);
+  int n_units = 0;
+  if (st == SR_OK) {
+    p->sess[0].unit_begin = 0;
+    n_units = s->cfg.n_heads * p->sess[0].nqb;
+    p->n_sess = 1;
+    p->n_heads = s->cfg.n_heads;
+    p->scale_log2 = s->scale * 1.4426950408889634f;
+    p->lse_ld = lse ? static_cast<int32_t>(s->lq) : 0;
+    p->o = static_cast<__nv_bfloat16*>(o);
+    p->lse = lse;
+    p->err_word = s->buf.err_word;
+    p->timeout_ns = s->cfg.wait_timeout_ns;
+    cudaError_t e = sr::launch_attention_1(*p, s->cfg.head_dim, n_units, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) st = SR_ERR_CUDA;
+  }
+  delete p;
+  return st;
+}
+
+sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32_t step, const void* q,
+                                   const void* k, const void* v, const int64_t* q_off, void* o, float* lse,
+                                   void* stream) {
+  if (!sessions || n < 1 || n > SR_MAX_BATCH || !q || !k || !v || !o || !q_off) return SR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return SR_ERR_ALIGN;
+  const sr_session* s0 = sessions[0];
+  if (!s0 || q_off[0] != 0) return SR_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const sr_session* s = sessions[i];
+    if (!s || s->cfg.n_heads != s0->cfg.n_heads || s->cfg.head_dim != s0->cfg.head_dim || s->scale != s0->scale)
+      return SR_ERR_INVALID_ARG;
+    if (step < 0 || step >= s->cfg.n_steps) return SR_ERR_INVALID_ARG;
+    if (q_off[i + 1] - q_off[i] != s->lq) return SR_ERR_INVALID_ARG;
+  }
+  const int64_t total = q_off[n];
+  if (total > (int64_t(1) << 28)) return SR_ERR_INVALID_ARG;
+  // longest key range first, so the biggest units start in the first wave
+  int order[SR_MAX_BATCH];
+  for (int i = 0; i < n; ++i) order[i] = i;
+  auto lk = [&](int i) {
+    const sr_session* s = sessions[i];
+    return s->cfg.n_sink + std::min<int64_t>(s->n_committed, s->cfg.window_frames) * s->tokens_per_frame + s->lq;
+  };
+  std::stable_sort(order, order + n, [&](int a, int b) { return lk(a) > lk(b); });
+
+  auto* p = new (std::nothrow) sr::AttnParams<sr::kAttnMaxBatch>;
+  if (!p) return SR_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  const int64_t row_elems = static_cast<int64_t>(s0->cfg.n_heads) * s0->cfg.head_dim;
+  sr_status st = SR_OK;
+  if (!encode_rows(&p->qmap, q, total, row_elems)) st = SR_ERR_CUDA;
+  int units = 0;
+  for (int r = 0; st == SR_OK && r < n; ++r) {
+    const int i = order[r];
+    st = fill_session(p->sess[r], sessions[i], step, k, v, q_off[i]);
+    p->sess[r].unit_begin = units;
+    units += s0->cfg.n_heads * p->sess[r].nqb;
+  }
+  if (st == SR_OK) {
+    p->n_sess = n;
+    p->n_heads = s0->cfg.n_heads;
+    p->scale_log2 = s0->scale * 1.4426950408889634f;
+    p->lse_ld = lse ? static_cast<int32_t>(total) : 0;
+    p->o = static_cast<__nv_bfloat16*>(o);
+    p->lse = lse;
+    p->err_word = s0->buf.err_word;
+    p->timeout_ns = s0->cfg.wait_timeout_ns;
+    cudaError_t e = sr::launch_attention_n(*p, s0->cfg.head_dim, units, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) st = SR_ERR_CUDA;
+  }
+  delete p;
+  return st;
+}
+
+sr_status sr_session_free(sr_session* s) {
+  delete s;
+  return SR_OK;
+}
+
+sr_status sr_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns, void* stream) {
+  if (!err_word || (reinterpret_cast<uintptr_t>(err_word) & 3u)) return SR_ERR_INVALID_ARG;
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return SR_ERR_INVALID_ARG;
+  cudaError_t e = sr::launch_debug_wait(err_word, timeout_ns, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SR_OK : SR_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// sr_kernels.h -- parameter blocks and launchers shared by the host API
+// (sr_api.cu) and the kernels. Internal to libsr.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sr.h"
+
+namespace sr {
+
+// ------------------------------------------------------------ attention
+// One session's view for one launch: three key/value segments (sink bank of
+// the step, occupied ring prefix, the chunk itself), each a 2D tensor map over
+// [rows][H*d] bf16 with a {64, 128} box and 128-byte swizzle. A segment with
+// zero rows has no map and contributes no tiles.
+struct alignas(128) AttnSession {
+  CUtensorMap kmap[3];
+  CUtensorMap vmap[3];
+  int32_t seg_rows[3];
+  int32_t q_row0;       // first row of this session in the packed q / o
+  int32_t lq;           // query rows
+  int32_t nqb;          // query blocks of 256 rows
+  int32_t unit_begin;   // first work unit (CTA) of this session
+  int32_t pad_;
+};
+
+template <int NSESS>
+struct alignas(128) AttnParams {
+  CUtensorMap qmap;               // packed q, [total_rows][H*d]
+  AttnSession sess[NSESS];
+  int32_t n_sess;
+  int32_t n_heads;
+  float scale_log2;               // softmax scale * log2(e)
+  int32_t lse_ld;                 // row stride of lse ([H][lse_ld]); 0 when lse is NULL
+  __nv_bfloat16* o;               // packed output, [total_rows][H][d]
+  float* lse;
+  int32_t* err_word;
+  uint64_t timeout_ns;
+};
+
+constexpr int kAttnThreads = 320;  // 8 softmax warps (2 groups), 1 MMA warp, 1 TMA warp
+constexpr int kAttnMaxBatch = SR_MAX_BATCH;
+
+int attn_smem_bytes(int head_dim);
+cudaError_t attn_prepare(int head_dim, int nsess_template);   // sets the smem attribute
+cudaError_t launch_attention_1(const AttnParams<1>& p, int head_dim, int n_units, cudaStream_t st);
+cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim, int n_units,
+                               cudaStream_t st);
+
+// ------------------------------------------------------------ RoPE / commit
+struct RopeParams {
+  double inv_freq[64];         // per rotary pair: base^(-2i/d_axis)
+  const __nv_bfloat16* src0;   // rotated
+  const __nv_bfloat16* src1;   // rotated (mode 0) or copied (mode 1)
+  __nv_bfloat16* dst0;
+  __nv_bfloat16* dst1;
+  int32_t* slot_frame;         // mode 1 only
+  int64_t n_committed;         // frames committed before this chunk
+  int32_t n_tok;               // F*T
+  int32_t n_heads;
+  int32_t tokens_per_frame;    // T
+  int32_t grid_w;
+  int32_t window_frames;       // W (mode 1)
+  int32_t chunk_frames;        // F (mode 1)
+  int32_t t_clock0;
+  int32_t mode;                // 0: rotate src0->dst0 and src1->dst1 in place; 1: commit
+  int8_t axis[64];             // 0 = t, 1 = h, 2 = w
+};
+
+cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st);
+
+// ------------------------------------------------------------ misc
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);
+cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, cudaStream_t st);
+cudaError_t launch_debug_wait(int32_t* err_word, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace sr

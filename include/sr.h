@@ -1,0 +1,187 @@
+/*
+ * sr.h -- C ABI of the streaming chunk-attention library (libsr.so), GB300 / sm_103a.
+ *
+ * The operations follow the streaming loop of the StreamRender-H3 project page
+ * ("Interactive Coding Worlds with Real-time Streaming Diffusion Render", NVlabs
+ * Sol-Engine), cited below as [H3 page]:
+ *   - condition once per session: the static context (sink) keys/values exist
+ *     once per denoising step, for the whole session, and every chunk reads them
+ *     ([H3 page] section 3.3 "Static-context KV caching");
+ *   - two denoising steps per chunk ([H3 page] 3.1.3 "Two-step generation"), each
+ *     attending bidirectionally over sink + recent history + the chunk itself
+ *     ([H3 page] 3.1.2);
+ *   - after the last step the chunk's keys receive their rotary position once and
+ *     are written in place into a preallocated ring buffer, evicting the oldest
+ *     frames ([H3 page] 3.2 Iteration 3 item 2; 3.3 "Persistent KV layout").
+ *
+ * Conventions shared by every call
+ *   - Tensors are bf16, token-major [L][H][d], contiguous: row stride H*d elements.
+ *     Every device pointer must be 16-byte aligned.
+ *   - All calls are asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream) and enqueue in call order.
+ *   - The library never allocates or frees device memory and never synchronises
+ *     a stream: every device buffer is owned by the caller and must outlive the
+ *     session; they are kept in the layout the attention kernel loads, so nothing
+ *     is repacked between calls ([H3 page] 3.3 "Persistent KV layout"). The only
+ *     host allocation is the session handle.
+ *   - Arguments are validated before anything is launched; a rejected call
+ *     changes no state. A failed launch returns SR_ERR_CUDA.
+ *   - Device-side waits are bounded. A wait that runs out of time writes a
+ *     nonzero code into the caller's err_word (first error wins) and the kernel
+ *     returns; the caller reads err_word after synchronising and may map it with
+ *     sr_device_error_status().
+ *   - A session is not thread-safe; distinct sessions are independent.
+ */
+#ifndef SR_H_
+#define SR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SR_API __attribute__((visibility("default")))
+#else
+#define SR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sr_session sr_session;   /* opaque host handle */
+
+typedef enum {
+  SR_OK = 0,
+  SR_ERR_INVALID_ARG = -1,   /* NULL pointer, bad size, step out of range, ... */
+  SR_ERR_UNSUPPORTED = -2,   /* e.g. head_dim other than 64 or 128 */
+  SR_ERR_ALIGN = -3,         /* a device pointer is not 16-byte aligned */
+  SR_ERR_STATE = -4,         /* call not allowed in the session's current state */
+  SR_ERR_CUDA = -5,          /* a CUDA runtime/driver call or a launch failed */
+  SR_ERR_TIMEOUT = -6        /* a device wait ran out of time (from err_word) */
+} sr_status;
+
+/* Device error codes written into err_word (0 = no error). */
+enum {
+  SR_DEVERR_NONE = 0,
+  SR_DEVERR_WAIT_TIMEOUT = 1  /* low 8 bits; bits 8..15 name the wait site */
+};
+
+/* Session shape and constants. */
+typedef struct {
+  int32_t n_heads;          /* H >= 1 */
+  int32_t head_dim;         /* d: 64 or 128 */
+  int32_t grid_h, grid_w;   /* latent grid; T = grid_h*grid_w tokens per frame, row-major (h, w) */
+  int32_t chunk_frames;     /* F >= 1 latent frames per chunk; Lq = F*T queries */
+  int32_t window_frames;    /* W: ring capacity in frames; 0 (no history) or >= F */
+  int32_t n_sink;           /* S >= 0 sink tokens per denoising step */
+  int32_t n_steps;          /* number of denoising steps = number of sink banks, >= 1 */
+  int32_t t_clock0;         /* rotary time position of stream frame 0 */
+  float rope_base;          /* rotary base (e.g. 10000); > 1 */
+  float softmax_scale;      /* <= 0 selects 1/sqrt(head_dim) */
+  uint64_t wait_timeout_ns; /* bound on every device-side wait; 0 selects 2 s */
+} sr_config;
+
+/* Caller-owned device buffers of one session (all 16-byte aligned). */
+typedef struct {
+  void* sink_k;             /* [n_steps][S][H][d] bf16: static context bank, final (no RoPE applied by the library) */
+  void* sink_v;             /* [n_steps][S][H][d] bf16 */
+  void* ring_k;             /* [W*T][H][d] bf16: rotated keys of committed frames, slot s = rows [s*T, (s+1)*T) */
+  void* ring_v;             /* [W*T][H][d] bf16 */
+  int32_t* slot_frame;      /* [W] int32: absolute frame held by each slot, -1 = empty */
+  int32_t* err_word;        /* [1] int32: device error word (see SR_DEVERR_*) */
+} sr_buffers;
+
+/*
+ * Create a session. Copies the sink banks from sink_k_src / sink_v_src (device,
+ * same layout as the bank) into bufs->sink_k / sink_v when they are non-NULL
+ * (NULL: the bank already holds them), fills slot_frame with -1, clears
+ * err_word and sets the committed-frame count n to 0. The static context is
+ * written once ([H3 page] 3.3 "Static-context KV caching", "Persistent KV layout").
+ * On success *out receives the handle; on failure *out is left NULL.
+ */
+SR_API sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs,
+                          const void* sink_k_src, const void* sink_v_src,
+                          void* stream, sr_session** out);
+
+/*
+ * Declare that the caller has put the ring into the state reached after
+ * n_committed frames (checkpoint / resume, or a synthetic mid-stream start):
+ * frame g in slot g mod W for the last min(n_committed, W) frames, and
+ * slot_frame filled accordingly. Only the host mirror of n changes.
+ */
+SR_API sr_status sr_session_restore(sr_session* s, int64_t n_committed);
+
+/* Frames committed so far (host mirror of the ring state). */
+SR_API sr_status sr_session_frames(const sr_session* s, int64_t* n_committed);
+
+/*
+ * In-place 3D (t, h, w) rotary positions on the chunk's queries and keys
+ * ([H3 page] 3.2 Iteration 3 item 2 and Iteration 4: absolute latent-frame
+ * time, so that a score is a function of the time gap only).
+ * q, k: [F*T][H][d] bf16, rotated in place. Token n lies in frame f = n / T,
+ * row (n % T) / grid_w, column n % grid_w; its time is t_clock0 + n_committed + f.
+ * The head dim splits into [d_t | d_h | d_w], d_h = d_w = 2*floor(d/6); inside an
+ * axis, pair (x[2i], x[2i+1]) turns by p * rope_base^(-2i/d_axis). Computed in
+ * fp32, stored bf16 round-to-nearest-even. Either pointer may be NULL to skip it.
+ */
+SR_API sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream);
+
+/*
+ * Attention of the chunk's queries for denoising step `step`
+ * ([H3 page] 3.1.2: bidirectional inside the window; "Prefix cache": the moving
+ * rows see every key of the window; 3.3: each step reads its own bank):
+ *   O = softmax(scale * Q K^T) V  over  sink bank[step] U occupied ring slots U chunk.
+ * q, k, v: [F*T][H][d] bf16 (q and k already rotated); o: [F*T][H][d] bf16 output.
+ * lse: optional [H][F*T] fp32 natural-log sum-exp of the scaled scores (NULL to skip).
+ * bf16 operands, fp32 accumulation and fp32 online softmax on the tensor cores.
+ */
+SR_API sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const void* k,
+                             const void* v, void* o, float* lse, void* stream);
+
+/*
+ * Commit the clean chunk after the last denoising step ([H3 page] 3.2 Iteration 3
+ * item 2: the rotary position is applied a single time, at the store into the
+ * frame's fixed slot; 3.3 "Persistent KV layout": the cache is modified where it
+ * lives). k_raw (un-rotated) and v:
+ * [F*T][H][d] bf16. Frame g = n + f goes to slot g mod W with its keys rotated at
+ * time t_clock0 + g; slot_frame[g mod W] = g; then n += F. The frames previously
+ * held by those slots are evicted. With W = 0 only n advances.
+ */
+SR_API sr_status sr_cache_commit(sr_session* s, const void* k_raw, const void* v, void* stream);
+
+/* Free the host handle (device buffers stay the caller's). NULL is accepted. */
+SR_API sr_status sr_session_free(sr_session* s);
+
+/*
+ * One launch for several sessions' chunks (multi-session serving; the page's
+ * per-request cache banks and reused attention metadata, [H3 page] 3.3).
+ * sessions[0..n-1] must share n_heads, head_dim and softmax scale. q, k, v, o are
+ * packed along L: session i owns rows [q_off[i], q_off[i+1]) (q_off is a HOST
+ * array of n+1 offsets, q_off[0] = 0, q_off[i+1]-q_off[i] = that session's F*T).
+ * Each session attends over its own bank[step], its own ring and its own rows.
+ * lse (optional) is [H][q_off[n]] fp32. 1 <= n <= SR_MAX_BATCH.
+ */
+#define SR_MAX_BATCH 16
+SR_API sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32_t step,
+                                   const void* q, const void* k, const void* v,
+                                   const int64_t* q_off, void* o, float* lse, void* stream);
+
+/* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
+SR_API sr_status sr_device_error_status(int32_t err_word_value);
+
+/*
+ * Diagnostic for the bounded-wait path: launches one block that waits on a
+ * barrier nothing will ever complete, using the same bounded wait as the
+ * kernels. After timeout_ns it writes SR_DEVERR_WAIT_TIMEOUT (site 0xFF) into
+ * *err_word (device, int32) and returns; no copy or tensor-core operation is in
+ * flight. Used to test failure detection without faulting or hanging a GPU.
+ */
+SR_API sr_status sr_debug_wait_timeout(int32_t* err_word, uint64_t timeout_ns, void* stream);
+
+/* Static string for a status code. */
+SR_API const char* sr_status_string(sr_status st);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SR_H_ */

@@ -13,8 +13,9 @@ What it computes, and where the pages define it. The pages are
              model paints the rest".
 
 * ``attention``  softmax(scale * Q K^T) V over the visible set with no mask:
-  attention inside the window is bidirectional ([H3-page] section 3.1.2), the
-  moving rows attend to the entire window ([H3-page] 3.1.2 "Prefix cache").
+  a chunk is denoised with two-way attention over its whole window
+  ([H3-page] section 3.1.2) and its rows see every key of that window
+  ([H3-page] 3.1.2 "Prefix cache").
 * ``rope``       3D (t, h, w) rotary positions applied once, at the absolute
   latent-frame index of the stream ([H3-page] 3.2 Iteration 3 item 2 and
   Iteration 4).

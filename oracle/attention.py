@@ -4,10 +4,9 @@ For each head and each query row i of the chunk:
     s_ij = scale * q_i . k_j           over every visible key j
     p_ij = exp(s_ij - max_j s_ij) / sum_j exp(s_ij - max_j s_ij)
     o_i  = sum_j p_ij v_j,             lse_i = max_j s_ij + ln sum_j exp(...)
-No mask: attention inside the window is bidirectional and the moving rows
-(the chunk) attend to the entire window ([H3-page] "Interactive Coding Worlds
-with Real-time Streaming Diffusion Render", section 3.1.2 and its "Prefix
-cache" paragraph). The visible set is assembled by the caller (see
+No mask: the chunk's rows see every key of the window, earlier or later
+([H3-page] "Interactive Coding Worlds with Real-time Streaming Diffusion
+Render", section 3.1.2 and its "Prefix cache" paragraph). The visible set is assembled by the caller (see
 ``session.py``). The score matrix is built query block by query block only to
 bound memory; each block is the plain definition above.
 """

@@ -1,10 +1,10 @@
 """Rolling history ring of W latent frames (test infrastructure only).
 
 [H3-page] "Interactive Coding Worlds with Real-time Streaming Diffusion
-Render", section 3.2 Iteration 3 item 2: the key-value cache is a
-preallocated ring buffer; each new latent frame is written into its slot in
-place, never concatenated or re-partitioned. Section 3.3 "Persistent KV
-layout": only the dynamic region is updated in place.
+Render", section 3.2 Iteration 3 item 2: the cache is a ring allocated up
+front, and a new latent frame overwrites one fixed slot of it rather than
+being appended. Section 3.3 "Persistent KV layout": the changing part of the
+cache is modified where it lives.
 
 Frame g (absolute index in the stream) goes to slot g mod W; writing it
 evicts whatever frame the slot held (the frame g - W). ``slot_frame[s]`` is

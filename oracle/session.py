@@ -3,7 +3,7 @@
 The calls follow the streaming loop of [H3-page] "Interactive Coding Worlds
 with Real-time Streaming Diffusion Render":
   * session set-up: one static-context (sink) K/V bank per denoising step,
-    computed once and reused for every later chunk (section 3.3
+    made at the start of the session and read by every chunk after (section 3.3
     "Static-context KV caching"; [teardown] "A window that slides, and a
     prefix that doesn't": text rows carry the timestep, so the steps cannot
     share a bank);

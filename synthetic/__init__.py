@@ -162,3 +162,33 @@ def plant_keys(q_bits: np.ndarray, k_bits: np.ndarray, every: int = 97, gain: fl
     idx = torch.arange(0, q.shape[0], every)
     k[idx] = q[idx] * gain
     return torch_to_bits(k.to(torch.bfloat16))
+
+
+def device_normal_bf16(shape, device, config: int, session: int = 0, chunk: int = 0, step: int = 0,
+                       tensor_id: int = 0, base_seed: int = 0):
+    """Seeded standard normal bf16 tensor drawn on the device (torch's CUDA
+    generator), for long runs where host-side draws would dominate. The same
+    seed tuple always gives the same bits; callers copy slices to the host
+    when the oracle needs them."""
+    seed = int(np.random.SeedSequence([base_seed, config, session, chunk, step, tensor_id, 7919])
+               .generate_state(1, dtype=np.uint64)[0] & ((1 << 63) - 1))
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def chunk_inputs_device(shape: Shape, config: int, device, session: int = 0, chunk: int = 0,
+                        base_seed: int = 0, with_steps: bool = True):
+    """Device-side counterpart of ``chunk_inputs`` (different bits, same recipe).
+    Returns dict with lists q, k, v (per step, empty if not with_steps) and
+    clean_k, clean_v as torch bf16 tensors on ``device``."""
+    dims = (shape.lq, shape.n_heads, shape.head_dim)
+    out = {"q": [], "k": [], "v": []}
+    if with_steps:
+        for s in range(shape.n_steps):
+            out["q"].append(device_normal_bf16(dims, device, config, session, chunk, s, T_Q, base_seed))
+            out["k"].append(device_normal_bf16(dims, device, config, session, chunk, s, T_K, base_seed))
+            out["v"].append(device_normal_bf16(dims, device, config, session, chunk, s, T_V, base_seed))
+    out["clean_k"] = device_normal_bf16(dims, device, config, session, chunk, 0, T_CLEAN_K, base_seed)
+    out["clean_v"] = device_normal_bf16(dims, device, config, session, chunk, 0, T_CLEAN_V, base_seed)
+    return out

@@ -5,7 +5,8 @@ slot table and against a deque brute force of "the last W frames".
 Session: the visible-set size of the H3 project page's worked example
 (tests/golden/decoder_window_visible_set.txt), causality (frames already
 evicted and future chunks change nothing), and clock-shift invariance of
-the scores (the Iteration 4 fix: scores depend only on time differences).
+the scores (the Iteration 4 fix: a score is a function of the gap in time,
+not of absolute time).
 """
 import collections
 import math
