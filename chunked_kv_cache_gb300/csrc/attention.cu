@@ -5,30 +5,40 @@
 // with no mask: every chunk query sees every visible key, in both time
 // directions (H3 project page, "Interactive Coding Worlds with Real-time
 // Streaming Diffusion Render", section 3.1.2 and its "Prefix cache"
-// paragraph, where the non-prefix rows see the whole window); each denoising step reads its own static-context
-// bank (section 3.3 "Static-context KV caching"); cache slots that are still
-// empty are simply not visited, so no mask is needed (section 3.2 Iteration 3
-// item 4, the seqused_k idea).
+// paragraph, where the non-prefix rows see the whole window); each denoising
+// step reads its own static-context bank (section 3.3 "Static-context KV
+// caching"); cache slots that are still empty are simply not visited, so no
+// mask is needed (section 3.2 Iteration 3 item 4, the seqused_k idea).
 //
-// One CTA = one work unit = (session, head, 256 query rows as two 128-row
-// tiles Q0, Q1 sharing every K/V tile). Warp roles:
-//   warps 0-3  softmax group 0: thread i owns row i of Q0
-//   warps 4-7  softmax group 1: thread i owns row i of Q1
-//   warp 8     MMA issuer (one thread): tcgen05.mma, accumulators in TMEM
-//   warp 9     TMA producer (one thread): Q once, then K/V tiles through an
-//              NSTAGE-deep shared-memory ring
+// One CTA = one work unit = (session, head, block of 256 query rows). A full
+// block is two 128-row tiles Q0, Q1 that share every K/V tile. The last block
+// of a chunk may hold a single tile; then the two softmax groups take the two
+// halves of the key range of that one tile ("split" mode) and merge their
+// partial results at the end, so the tensor pipe still alternates between
+// two independent score tiles. Units run longest first: all full blocks, then
+// all last blocks.
+//
+// Warp roles:
+//   warps 0-3   softmax group 0 (thread i owns row i of its tile)
+//   warps 4-7   softmax group 1
+//   warp 8      MMA issuer (one thread): tcgen05.mma, accumulators in TMEM
+//   warp 9      TMA producer (one thread): Q once, then K/V tiles through an
+//               NSTAGE-deep shared-memory ring, in the order the MMA consumes
+//   warps 10-11 idle (they complete the third warpgroup)
+// Registers: launched at 168 per thread (384 x 168 = 64512); the third
+// warpgroup gives back down to 72 and the two softmax warpgroups take 216
+// each: 2 x 128 x 216 + 128 x 72 = 64512, the launch's total.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) fp32 scores, O0 [256,256+d)
 // O1 [384,384+d) fp32 accumulators. P (bf16) is written back over the first
 // 64 columns of its S region and fed to the PV MMA straight from TMEM.
 //
-// Issue order of the MMA thread, i = KV tile:
+// Issue order of the MMA thread, i = iteration:
 //   S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 PV1_1 S1_2 | ...
 // so while softmax group 0 works on S0_i the tensor pipe runs PV1_{i-1} and
-// S1_i, and the other way round (two query tiles ping-pong on one SM).
-// Online softmax in fp32 with exp2 and the scale folded into one FMA; the
-// running maximum is only raised (and O rescaled in TMEM) when a new tile
-// exceeds it by more than 2^8, which keeps numerator and denominator exact
-// and avoids most rescales.
+// S1_i, and the other way round. Online softmax in fp32 with exp2 and the
+// scale folded into one packed FMA; the running maximum is only raised (and O
+// rescaled in TMEM) when a new tile exceeds it by more than 2^8, which keeps
+// numerator and denominator consistent and avoids most rescales.
 #include <cuda_bf16.h>
 
 #include "sr_device.cuh"
@@ -42,6 +52,11 @@ constexpr int BM = 128;      // rows per query tile
 constexpr int BN = 128;      // keys per K/V tile
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 72;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kAttnThreads * kLaunchRegs,
+              "register split exceeds what the block is launched with");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -53,7 +68,7 @@ struct Cfg {
   static constexpr int kStages = D == 128 ? 4 : 6;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemKV = kStages * kTileBytes;
-  static constexpr int kSmemBar = 1024;
+  static constexpr int kSmemBar = 2048;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kSmemBar + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 1);
@@ -69,12 +84,9 @@ struct SmemBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  float xm[BM];   // split mode: group 1's running max / sum, handed to group 0
+  float xl[BM];
 };
-
-// Load-sequence index of K_j and V_j (the producer loads in the order the MMA
-// thread consumes: K0, K1, V0, K2, V1, ..., K_{n-1}, V_{n-2}, V_{n-1}).
-__device__ __forceinline__ int seq_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
-__device__ __forceinline__ int seq_v(int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; }
 
 struct TileMap {
   int nt[3];
@@ -88,6 +100,39 @@ struct TileMap {
   }
 };
 
+// The key tiles each query tile walks: in shared mode both walk all n tiles;
+// in split mode tile 0 walks [0, h) and tile 1 walks [h, n).
+struct Walk {
+  bool split;
+  int n, h;
+  __device__ __forceinline__ int count(int t) const { return split ? (t == 0 ? h : n - h) : n; }
+  __device__ __forceinline__ int kv(int t, int i) const { return (split && t == 1) ? h + i : i; }
+  __device__ __forceinline__ int iters() const { return split ? h : n; }
+};
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int NSESS>
+__device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, int H, int& si, int& head,
+                                            int& qb) {
+  if (u < p.n_full_units) {
+    si = 0;
+#pragma unroll 1
+    while (si + 1 < p.n_sess && u >= p.sess[si].unit_begin + H * (p.sess[si].nqb - 1)) ++si;
+    const int local = u - p.sess[si].unit_begin;
+    const int nf = p.sess[si].nqb - 1;
+    head = local / nf;
+    qb = local % nf;
+  } else {
+    const int t = u - p.n_full_units;
+    si = t / H;                       // every session has exactly H last-block units
+    head = t - si * H;
+    qb = p.sess[si].nqb - 1;
+  }
+}
+
 template <int D, int NSESS>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams<NSESS> p) {
   using C = Cfg<D>;
@@ -100,20 +145,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // ---- work unit -> (session, head, query block)
-  int si = 0;
-#pragma unroll 1
-  while (si + 1 < p.n_sess && static_cast<int>(blockIdx.x) >= p.sess[si + 1].unit_begin) ++si;
+  int si, head, qb;
+  decode_unit(p, static_cast<int>(blockIdx.x), p.n_heads, si, head, qb);
   const AttnSession& S = p.sess[si];
-  const int u = blockIdx.x - S.unit_begin;
-  const int head = u / S.nqb;
-  const int qb = u % S.nqb;
   const int q_local0 = qb * 2 * BM;                       // first query row of the unit (session-local)
   const int n_qtiles = min(2, (S.lq - q_local0 + BM - 1) / BM);
   TileMap tm;
 #pragma unroll
   for (int s = 0; s < 3; ++s) tm.nt[s] = (S.seg_rows[s] + BN - 1) / BN;
   const int n_kv = tm.nt[0] + tm.nt[1] + tm.nt[2];
+  const Walk wk{n_qtiles == 1, n_kv, n_qtiles == 1 ? (n_kv + 1) / 2 : n_kv};
 
   WaitCtx wc{&bars->abort, p.err_word, p.timeout_ns};
 
@@ -141,9 +182,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp >= 8) {
+    regs_dec<kRegsOther>();
+    if (warp == kTmaWarp && lane == 0) {
+      // ---------------------------------------------------------- producer
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       tma_prefetch_map(&p.qmap);
@@ -157,23 +199,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_2d(sQ + t * C::kTileBytes + a * C::kAtomBytes, &p.qmap, &bars->q_full,
                       head * D + a * 64, S.q_row0 + q_local0 + t * BM, pol_q);
-      const int n_loads = 2 * n_kv;
-      int issued = 0;
-      for (int idx = 0; idx < n_loads; ++idx) {
+      int idx = 0;
+      bool ok = true;
+      auto load = [&](bool is_v, int j) {
+        if (!ok) return;
         const int stage = idx % C::kStages;
-        if (idx >= C::kStages && !wait_bounded(&bars->kv_empty[stage], ((idx / C::kStages) - 1) & 1, wc, 1))
-          break;
-        // which tile: idx 0 -> K0; odd idx 2j-1 -> K_j (j >= 1); even idx 2j+2 -> V_j; last -> V_{n-1}
-        int j;
-        bool is_v;
-        if (idx == 0) {
-          j = 0; is_v = false;
-        } else if (idx == n_loads - 1) {
-          j = n_kv - 1; is_v = true;
-        } else if (idx & 1) {
-          j = (idx + 1) / 2; is_v = false;
-        } else {
-          j = idx / 2 - 1; is_v = true;
+        if (idx >= C::kStages && !wait_bounded(&bars->kv_empty[stage], ((idx / C::kStages) - 1) & 1, wc, 1)) {
+          ok = false;
+          return;
         }
         int seg, row0;
         tm.locate(j, seg, row0);
@@ -182,28 +215,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         uint8_t* dst = sKV + stage * C::kTileBytes;
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_2d(dst + a * C::kAtomBytes, map, &bars->kv_full[stage], head * D + a * 64, row0, pol_kv);
-        issued = idx + 1;
+        ++idx;
+      };
+      // per iteration: the K tiles of iteration i, then the V tiles of i - 1
+      auto loads_of = [&](bool is_v, int i) {
+        if (wk.split) {
+          for (int t = 0; t < 2; ++t)
+            if (i < wk.count(t)) load(is_v, wk.kv(t, i));
+        } else {
+          load(is_v, i);
+        }
+      };
+      const int n_it = wk.iters();
+      for (int i = 0; i < n_it && ok; ++i) {
+        loads_of(false, i);
+        if (i > 0) loads_of(true, i - 1);
       }
-      if (bars->abort) {
+      loads_of(true, n_it - 1);
+      if (!ok || bars->abort) {
         // let every copy this CTA started land before shared memory is released
         wait_drain(&bars->q_full, 0, p.timeout_ns);
-        for (int idx = max(0, issued - C::kStages); idx < issued; ++idx)
-          wait_drain(&bars->kv_full[idx % C::kStages], (idx / C::kStages) & 1, p.timeout_ns);
+        for (int k = max(0, idx - C::kStages); k < idx; ++k)
+          wait_drain(&bars->kv_full[k % C::kStages], (k / C::kStages) & 1, p.timeout_ns);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       bool issued_any = false;
       bool ok = wait_bounded(&bars->q_full, 0, wc, 2);
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
+      int c = 0;   // consume counter, same order as the producer's loads
+      auto take = [&](int& stage) {
+        stage = c % C::kStages;
+        if (ok && !wait_bounded(&bars->kv_full[stage], (c / C::kStages) & 1, wc, 3)) ok = false;
+        ++c;
+      };
+      auto takes = [&](int i, int (&st)[2]) {
+        if (wk.split) {
+          for (int t = 0; t < 2; ++t)
+            if (i < wk.count(t)) take(st[t]);
+        } else {
+          take(st[0]);
+          st[1] = st[0];
+        }
+      };
       auto qk = [&](int t, int stage) {   // S_t = Q_t K^T
         const uint32_t d_tmem = tmem + t * BN;
+        const uint32_t qt = sq + (wk.split ? 0 : t) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kAtomBytes + (kk % 4) * 32;
-          const uint64_t ad = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
+          const uint64_t ad = sdesc_sw128(qt + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(skv + stage * C::kTileBytes + off, 16, 1024);
           mma_ss(d_tmem, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
         }
@@ -217,62 +279,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           mma_ts(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      const bool two = n_qtiles == 2;
-      if (ok) {
-        const int sk = seq_k(0) % C::kStages;
-        ok = wait_bounded(&bars->kv_full[sk], (seq_k(0) / C::kStages) & 1, wc, 3);
-        if (ok) {
-          tc_fence_after();
-          qk(0, sk);
-          tc_commit(&bars->s_full[0]);
-          if (two) {
-            qk(1, sk);
-            tc_commit(&bars->s_full[1]);
-          }
-          tc_commit(&bars->kv_empty[sk]);
-          issued_any = true;
-        }
-      }
-      for (int j = 1; ok && j < n_kv; ++j) {
-        const int ik = seq_k(j), iv = seq_v(j - 1, n_kv);
-        const int sk = ik % C::kStages, sv = iv % C::kStages;
-        if (!wait_bounded(&bars->kv_full[sk], (ik / C::kStages) & 1, wc, 3)) { ok = false; break; }
-        if (!wait_bounded(&bars->kv_full[sv], (iv / C::kStages) & 1, wc, 3)) { ok = false; break; }
-        if (!wait_bounded(&bars->p_full[0], (j - 1) & 1, wc, 4)) { ok = false; break; }
+      const int n_it = wk.iters();
+      int ks[2] = {0, 0}, vs[2] = {0, 0};
+      for (int i = 0; ok && i <= n_it; ++i) {
+        if (i < n_it) takes(i, ks);
+        if (i > 0) takes(i - 1, vs);
+        if (!ok) break;
         tc_fence_after();
-        pv(0, sv, j - 1 > 0);
-        qk(0, sk);
-        tc_commit(&bars->s_full[0]);
-        if (two) {
-          if (!wait_bounded(&bars->p_full[1], (j - 1) & 1, wc, 4)) { ok = false; break; }
-          tc_fence_after();
-          pv(1, sv, j - 1 > 0);
-        }
-        tc_commit(&bars->kv_empty[sv]);
-        if (two) {
-          qk(1, sk);
-          tc_commit(&bars->s_full[1]);
-        }
-        tc_commit(&bars->kv_empty[sk]);
-      }
-      if (ok) {
-        const int iv = seq_v(n_kv - 1, n_kv);
-        const int sv = iv % C::kStages;
-        ok = wait_bounded(&bars->kv_full[sv], (iv / C::kStages) & 1, wc, 3) &&
-             wait_bounded(&bars->p_full[0], (n_kv - 1) & 1, wc, 4);
-        if (ok) {
-          tc_fence_after();
-          pv(0, sv, n_kv > 1);
-          tc_commit(&bars->o_done[0]);
-          if (two) {
-            ok = wait_bounded(&bars->p_full[1], (n_kv - 1) & 1, wc, 4);
-            if (ok) {
-              tc_fence_after();
-              pv(1, sv, n_kv > 1);
-              tc_commit(&bars->o_done[1]);
+        for (int t = 0; t < 2; ++t) {
+          const int cnt = wk.count(t);
+          if (i > 0 && i - 1 < cnt) {
+            if (!wait_bounded(&bars->p_full[t], (i - 1) & 1, wc, 4)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+            pv(t, vs[t], i - 1 > 0);
+            if (i - 1 == cnt - 1) tc_commit(&bars->o_done[t]);
+            if (wk.split) tc_commit(&bars->kv_empty[vs[t]]);
           }
-          tc_commit(&bars->kv_empty[sv]);
+          if (i < cnt) {
+            qk(t, ks[t]);
+            tc_commit(&bars->s_full[t]);
+            if (wk.split) tc_commit(&bars->kv_empty[ks[t]]);
+            issued_any = true;
+          }
+        }
+        if (ok && !wk.split) {
+          if (i > 0) tc_commit(&bars->kv_empty[vs[0]]);
+          if (i < n_it) tc_commit(&bars->kv_empty[ks[0]]);
         }
       }
       if (!ok && issued_any) {
@@ -282,6 +317,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       }
     }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax groups
     const int t = warp / 4;
     const int row = threadIdx.x % BM;
@@ -289,10 +325,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     const uint32_t t_s = tmem + lane_base + t * BN;
     const uint32_t t_o = tmem + lane_base + 256 + t * 128;
     const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     float m = -INFINITY;   // running max of scaled scores, log2 units
     float l = 0.f;         // running sum of exp2(score - m)
-    bool ok = t < n_qtiles;
-    for (int j = 0; ok && j < n_kv; ++j) {
+    const int cnt = wk.count(t);
+    bool ok = true;
+    for (int j = 0; ok && j < cnt; ++j) {
       ok = wait_bounded(&bars->s_full[t], j & 1, wc, 5);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -306,87 +344,126 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       float* s = reinterpret_cast<float*>(&r[0][0]);
       // ragged tail of a segment: keys past its end are not part of the window
       int seg, row0;
-      tm.locate(j, seg, row0);
+      tm.locate(wk.kv(t, j), seg, row0);
       const int valid = S.seg_rows[seg] - row0;
       if (valid < BN) {
 #pragma unroll
         for (int i = 0; i < BN; ++i)
           if (i >= valid) s[i] = -INFINITY;
       }
-      float mx[8];
+      float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]), a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int i = 8; i < BN; ++i) mx[i % 8] = fmaxf(mx[i % 8], s[i]);
-      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      mt *= sl2;
+      for (int i = 8; i < BN; i += 8) {
+        a0 = fmax3(a0, s[i], s[i + 1]);
+        a1 = fmax3(a1, s[i + 2], s[i + 3]);
+        a2 = fmax3(a2, s[i + 4], s[i + 5]);
+        a3 = fmax3(a3, s[i + 6], s[i + 7]);
+      }
+      const float mt = fmax3(a0, a1, fmaxf(a2, a3)) * sl2;
       const bool need = (j == 0) || (mt > m + kRescaleThreshold);
-      if (__any_sync(0xffffffffu, need)) {
+      float f = 1.f;                    // factor that takes O and l to the new maximum
+      const bool rescale = __any_sync(0xffffffffu, need);
+      if (rescale) {
         const float m_new = fmaxf(m, mt);
-        if (j > 0) {
-          // O was last written by PV_{j-1}, which completed before S_j was
-          // signalled (in-order tensor pipe + commit covers all prior MMAs).
-          const float f = ex2_approx(m - m_new);
-          l *= f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
-            tmem_wait_ld();
-            tmem_fix(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tmem_st32(t_o + c * 32, o);
-          }
-        }
+        if (j > 0) f = ex2_approx(m - m_new);
         m = m_new;
       }
-      const float neg_m = -m;
-      float ls[8];
+      const float2 negm = make_float2(-m, -m);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
-      uint32_t pk[2][32];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < BN; i += 2) {
-        const float p0 = ex2_approx(fmaf(s[i], sl2, neg_m));
-        const float p1 = ex2_approx(fmaf(s[i + 1], sl2, neg_m));
-        ls[(i / 2) % 8] += p0 + p1;
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-        pk[(i / 2) / 32][(i / 2) % 32] = *reinterpret_cast<uint32_t*>(&b2);
+        for (int k = 0; k < 16; ++k) {
+          const int i = c * 32 + 2 * k;
+          const float2 x = __ffma2_rn(make_float2(s[i], s[i + 1]), sl2x2, negm);
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[k % 4] = __fadd2_rn(acc[k % 4], e);
+          pk[k] = pack_bf16x2(e.x, e.y);
+        }
+        tmem_st16(t_s + c * 16, pk);
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tmem_st32(t_s, pk[0]);
-      tmem_st32(t_s + 32, pk[1]);
+      const float2 s01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+      l = l * f + (s01.x + s01.y);
+      if (rescale && j > 0) {
+        // O was last written by PV_{j-1}, which completed before S_j was
+        // signalled (in-order tensor pipe; a commit covers all prior MMAs);
+        // PV_j is not issued before this thread arrives on p_full below.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c * 32, o);
+          tmem_wait_ld();
+          tmem_fix(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          tmem_st32(t_o + c * 32, o);
+        }
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[t]);
     }
-    if (ok) {
+
+    // ---- epilogue: normalise and store (in split mode group 0 merges both halves)
+    const int q_local = q_local0 + (wk.split ? 0 : t) * BM + row;
+    const bool live = q_local < S.lq;
+    const int64_t out_row = static_cast<int64_t>(S.q_row0) + q_local;
+    bool merge = false;
+    if (wk.split) {
+      if (t == 1) {
+        bars->xm[row] = (ok && cnt > 0) ? m : -INFINITY;
+        bars->xl[row] = (ok && cnt > 0) ? l : 0.f;
+      }
+      named_sync(1, 2 * 4 * 32);
+      merge = wk.count(1) > 0;
+    }
+    const bool writer = !wk.split || t == 0;
+    if (writer && ok) {
       ok = wait_bounded(&bars->o_done[t], 0, wc, 6);
+      if (ok && merge) ok = wait_bounded(&bars->o_done[1], 0, wc, 6);
       ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok) {
+    if (writer && ok) {
       tc_fence_after();
-      const int q_local = q_local0 + t * BM + row;
-      const bool live = q_local < S.lq;
+      float f0 = 1.f, f1 = 0.f;
+      if (merge) {
+        const float m1 = bars->xm[row], l1 = bars->xl[row];
+        const float mm = fmaxf(m, m1);
+        f0 = ex2_approx(m - mm);
+        f1 = ex2_approx(m1 - mm);
+        l = l * f0 + l1 * f1;
+        m = mm;
+      }
       const float inv_l = 1.f / l;
-      const int64_t out_row = static_cast<int64_t>(S.q_row0) + q_local;
+      f0 *= inv_l;
+      f1 *= inv_l;
       __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
+      const uint32_t t_o1 = tmem + lane_base + 256 + 128;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(t_o + c * 32, o);
         tmem_wait_ld();
         tmem_fix(o);
+        if (merge) {
+          uint32_t o1[32];
+          tmem_ld32(t_o1 + c * 32, o1);
+          tmem_wait_ld();
+          tmem_fix(o1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            o[i] = __float_as_uint(__uint_as_float(o[i]) * f0 + __uint_as_float(o1[i]) * f1);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f0);
+        }
         if (live) {
           uint4 pkt[4];
           uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[2 * i]) * inv_l,
-                                                      __uint_as_float(o[2 * i + 1]) * inv_l);
-            w[i] = *reinterpret_cast<uint32_t*>(&b2);
-          }
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) d4[i] = pkt[i];
@@ -405,8 +482,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   }
 }
 
+// The softmax warpgroups' setmaxnreg.inc can only be granted if the kernel is
+// launched with the registers the split assumes; refuse to launch otherwise
+// (an increase that cannot be granted would never return).
 template <int D, int NSESS>
 cudaError_t set_attr() {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, attn_kernel<D, NSESS>);
+  if (e != cudaSuccess) return e;
+  if (a.numRegs != kLaunchRegs || a.maxThreadsPerBlock < kAttnThreads) return cudaErrorInvalidConfiguration;
   return cudaFuncSetAttribute(attn_kernel<D, NSESS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Cfg<D>::kSmemBytes);
 }
@@ -438,10 +522,7 @@ cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim,
   return cudaGetLastError();
 }
 
-}  // namespace sr
-
 // ---------------------------------------------------------------- diagnostics
-namespace sr {
 namespace {
 // Waits on a barrier that nothing ever completes, with the same bounded wait
 // the attention kernel uses, so that the time-out path can be exercised
@@ -464,4 +545,5 @@ cudaError_t launch_debug_wait(int32_t* err_word, uint64_t timeout_ns, cudaStream
   debug_wait_kernel<<<1, 32, 0, st>>>(err_word, timeout_ns);
   return cudaGetLastError();
 }
+
 }  // namespace sr

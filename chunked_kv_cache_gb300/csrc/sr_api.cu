@@ -306,6 +306,7 @@ sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const v
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return SR_ERR_ALIGN;
+  if (ensure_attn_attr(s->cfg.head_dim, 1) != cudaSuccess) return SR_ERR_CUDA;
   auto* p = new (std::nothrow) sr::AttnParams<1>;
   if (!p) return SR_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
@@ -315,7 +316,10 @@ sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const v
   if (st == SR_OK) st = fill_session(p->sess[0], s, step, k, v, 0);
   int n_units = 0;
   if (st == SR_OK) {
+    // full 256-row blocks first (longest units), then the last block of every head
     p->sess[0].unit_begin = 0;
+    p->sess[0].tail_begin = 0;
+    p->n_full_units = s->cfg.n_heads * (p->sess[0].nqb - 1);
     n_units = s->cfg.n_heads * p->sess[0].nqb;
     p->n_sess = 1;
     p->n_heads = s->cfg.n_heads;
@@ -359,20 +363,27 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
   };
   std::stable_sort(order, order + n, [&](int a, int b) { return lk(a) > lk(b); });
 
+  if (ensure_attn_attr(s0->cfg.head_dim, sr::kAttnMaxBatch) != cudaSuccess) return SR_ERR_CUDA;
   auto* p = new (std::nothrow) sr::AttnParams<sr::kAttnMaxBatch>;
   if (!p) return SR_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   const int64_t row_elems = static_cast<int64_t>(s0->cfg.n_heads) * s0->cfg.head_dim;
   sr_status st = SR_OK;
   if (!encode_rows(&p->qmap, q, total, row_elems)) st = SR_ERR_CUDA;
-  int units = 0;
+  // units: every session's full 256-row blocks (sessions by decreasing key
+  // count), then every session's last block -- longest work first
+  int full = 0, tails = 0;
   for (int r = 0; st == SR_OK && r < n; ++r) {
     const int i = order[r];
     st = fill_session(p->sess[r], sessions[i], step, k, v, q_off[i]);
-    p->sess[r].unit_begin = units;
-    units += s0->cfg.n_heads * p->sess[r].nqb;
+    p->sess[r].unit_begin = full;
+    p->sess[r].tail_begin = tails;
+    full += s0->cfg.n_heads * (p->sess[r].nqb - 1);
+    tails += s0->cfg.n_heads;
   }
+  const int units = full + tails;
   if (st == SR_OK) {
+    p->n_full_units = full;
     p->n_sess = n;
     p->n_heads = s0->cfg.n_heads;
     p->scale_log2 = s0->scale * 1.4426950408889634f;

@@ -61,9 +61,10 @@ __device__ __forceinline__ void raise_error(const WaitCtx& w, int site) {
   atomicCAS(reinterpret_cast<int*>(w.err_word), 0, SR_DEVERR_WAIT_TIMEOUT | (site << 8));
 }
 
-// Returns false if the CTA aborted (this wait timed out or another one did).
-__device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of a bounded wait. Returns false if the CTA aborted (this wait
+// timed out or another one did). Inlined: the attention kernel's warpgroups
+// run under setmaxnreg, where calls are not allowed to carry live registers.
+__device__ __forceinline__ bool wait_bounded_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -74,10 +75,16 @@ __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const 
     }
   }
 }
+// Fast path: one try_wait (which itself suspends for a while in hardware)
+// before falling back to the timed loop.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const WaitCtx& w, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, w, site);
+}
 
 // Used only while tearing down after an abort: waits for this CTA's own
 // copies / MMAs in flight, ignoring the abort flag, again with a time limit.
-__device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) return false;
@@ -207,6 +214,37 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      SR_W8(0), SR_W8(8)
+      : "memory");
+}
+
+// Register reallocation between warpgroups (warpgroup-wide). The shares used
+// by the attention kernel add up to exactly what the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// max of three floats in one instruction (sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -23,8 +23,8 @@ struct alignas(128) AttnSession {
   int32_t q_row0;       // first row of this session in the packed q / o
   int32_t lq;           // query rows
   int32_t nqb;          // query blocks of 256 rows
-  int32_t unit_begin;   // first work unit (CTA) of this session
-  int32_t pad_;
+  int32_t unit_begin;   // first full-block unit of this session (full blocks come first)
+  int32_t tail_begin;   // index of this session's last-block units among all last-block units
 };
 
 template <int NSESS>
@@ -32,6 +32,7 @@ struct alignas(128) AttnParams {
   CUtensorMap qmap;               // packed q, [total_rows][H*d]
   AttnSession sess[NSESS];
   int32_t n_sess;
+  int32_t n_full_units;           // units of full 256-row blocks (all sessions); last blocks follow
   int32_t n_heads;
   float scale_log2;               // softmax scale * log2(e)
   int32_t lse_ld;                 // row stride of lse ([H][lse_ld]); 0 when lse is NULL
@@ -41,7 +42,7 @@ struct alignas(128) AttnParams {
   uint64_t timeout_ns;
 };
 
-constexpr int kAttnThreads = 320;  // 8 softmax warps (2 groups), 1 MMA warp, 1 TMA warp
+constexpr int kAttnThreads = 384;  // 2 softmax warpgroups, then MMA warp, TMA warp and 2 idle warps
 constexpr int kAttnMaxBatch = SR_MAX_BATCH;
 
 int attn_smem_bytes(int head_dim);
