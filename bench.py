@@ -56,6 +56,21 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Job time = the slowest rank's time (replicas run the same work)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job throughput of N replicas: every rank's units over the max time."""
+    return world * units_per_rank / seconds
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -201,18 +216,12 @@ def run_ours(args):
     for s, _ in sessions:
         if s.error_status() != 0:
             raise RuntimeError("device error word set during the bench")
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, dev)
 
     # end to end through the public API: pinned host inputs in, result out
     e2e = run_e2e(shape, args, dev, sessions[0][0]) if not args.profile else {"seconds": 1.0, "chunks": 0,
                                                                               "h2d": 0, "d2h": 0}
-    if world > 1:
-        t = torch.tensor([e2e["seconds"]], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e["seconds"] = float(t.item())
+    e2e["seconds"] = max_over_ranks(e2e["seconds"], dev)
     clocks = clk.summary()
     if rank != 0:
         if world > 1:
@@ -221,7 +230,7 @@ def run_ours(args):
     peak_tf, peak_gbs, peak_kind = _peaks()
     attn_avg = statistics.mean(attn_ms)
     achieved = flops_attn / (attn_avg / 1e3) / 1e12
-    value = world * args.steps * flops_chunk / elapsed / 1e12
+    value = aggregate_throughput(args.steps * flops_chunk, elapsed, world) / 1e12
     commit_avg = statistics.mean(commit_ms)
     rope_avg = statistics.mean(rope_ms)
     cpu = cpu_baseline(shape, args) if world == 1 and not args.profile else None
@@ -248,7 +257,8 @@ def run_ours(args):
                           "GB/s": round(commit_bytes / (rope_avg / 1e3) / 1e9, 1),
                           "frac_hbm": round(commit_bytes / (rope_avg / 1e3) / 1e9 / peak_gbs, 4)},
         },
-        "e2e": {"value": round(world * e2e["chunks"] * flops_chunk / e2e["seconds"] / 1e12, 2), "unit": UNIT,
+        "e2e": {"value": round(aggregate_throughput(e2e["chunks"] * flops_chunk, e2e["seconds"], world) / 1e12, 2),
+                "unit": UNIT,
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "cpu_baseline": cpu,
         "clocks": clocks,
