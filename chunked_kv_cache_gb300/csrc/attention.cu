@@ -65,18 +65,22 @@ struct Cfg {
   static constexpr int kAtoms = D / 64;                 // 128-byte swizzle atoms per row
   static constexpr int kAtomBytes = BM * 128;           // one [128 rows][64 cols] bf16 box
   static constexpr int kTileBytes = kAtoms * kAtomBytes;
-  static constexpr int kStages = D == 128 ? 4 : 6;
+  // K/V ring depth. In split mode the second Q slot is free and serves as one
+  // more stage (each iteration then needs four tiles: two K, two V).
+  static constexpr int kStages = D == 128 ? 5 : 6;
+  static constexpr int kStagesSplit = kStages + 1;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemKV = kStages * kTileBytes;
   static constexpr int kSmemBar = 2048;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + kSmemBar + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per block");
   static constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 1);
 };
 
 struct SmemBars {
   uint64_t q_full;
-  uint64_t kv_full[8];
+  uint64_t kv_full[8];    // up to kStagesSplit stages
   uint64_t kv_empty[8];
   uint64_t s_full[2];
   uint64_t p_full[2];
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kStagesSplit; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
@@ -201,10 +205,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                       head * D + a * 64, S.q_row0 + q_local0 + t * BM, pol_q);
       int idx = 0;
       bool ok = true;
+      const int nst = wk.split ? C::kStagesSplit : C::kStages;
       auto load = [&](bool is_v, int j) {
         if (!ok) return;
-        const int stage = idx % C::kStages;
-        if (idx >= C::kStages && !wait_bounded(&bars->kv_empty[stage], ((idx / C::kStages) - 1) & 1, wc, 1)) {
+        const int stage = idx % nst;
+        if (idx >= nst && !wait_bounded(&bars->kv_empty[stage], ((idx / nst) - 1) & 1, wc, 1)) {
           ok = false;
           return;
         }
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         tm.locate(j, seg, row0);
         const CUtensorMap* map = is_v ? &S.vmap[seg] : &S.kmap[seg];
         mbar_arrive_expect_tx(&bars->kv_full[stage], C::kTileBytes);
-        uint8_t* dst = sKV + stage * C::kTileBytes;
+        uint8_t* dst = stage < C::kStages ? sKV + stage * C::kTileBytes : sQ + C::kTileBytes;
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_2d(dst + a * C::kAtomBytes, map, &bars->kv_full[stage], head * D + a * 64, row0, pol_kv);
         ++idx;
@@ -235,8 +240,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       if (!ok || bars->abort) {
         // let every copy this CTA started land before shared memory is released
         wait_drain(&bars->q_full, 0, p.timeout_ns);
-        for (int k = max(0, idx - C::kStages); k < idx; ++k)
-          wait_drain(&bars->kv_full[k % C::kStages], (k / C::kStages) & 1, p.timeout_ns);
+        for (int k = max(0, idx - nst); k < idx; ++k)
+          wait_drain(&bars->kv_full[k % nst], (k / nst) & 1, p.timeout_ns);
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -245,10 +250,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
       int c = 0;   // consume counter, same order as the producer's loads
+      const int nst = wk.split ? C::kStagesSplit : C::kStages;
       auto take = [&](int& stage) {
-        stage = c % C::kStages;
-        if (ok && !wait_bounded(&bars->kv_full[stage], (c / C::kStages) & 1, wc, 3)) ok = false;
+        stage = c % nst;
+        if (ok && !wait_bounded(&bars->kv_full[stage], (c / nst) & 1, wc, 3)) ok = false;
         ++c;
+      };
+      // shared-memory address of a K/V stage (the extra split-mode stage is the second Q slot)
+      auto stage_addr = [&](int stage) -> uint32_t {
+        return stage < C::kStages ? skv + stage * C::kTileBytes : sq + C::kTileBytes;
       };
       auto takes = [&](int i, int (&st)[2]) {
         if (wk.split) {
@@ -266,7 +276,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kAtomBytes + (kk % 4) * 32;
           const uint64_t ad = sdesc_sw128(qt + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(skv + stage * C::kTileBytes + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(stage_addr(stage) + off, 16, 1024);
           mma_ss(d_tmem, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const uint32_t a_tmem = tmem + t * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(skv + stage * C::kTileBytes + kk * 16 * 128, C::kAtomBytes, 1024);
+          const uint64_t bd = sdesc_sw128(stage_addr(stage) + kk * 16 * 128, C::kAtomBytes, 1024);
           mma_ts(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
