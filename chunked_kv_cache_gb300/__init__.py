@@ -14,13 +14,13 @@ from . import _native
 from ._native import (SrConfig, SrBuffers, SrError, sr_session_init, sr_session_restore, sr_session_frames,
                       sr_rope3d_qk, sr_chunk_attention, sr_cache_commit, sr_session_free,
                       sr_chunk_attention_batch, sr_device_error_status, sr_debug_wait_timeout,
-                      SR_MAX_BATCH)
+                      sr_workspace_bytes, SR_MAX_BATCH)
 
 __all__ = [
     "Session", "chunk_attention_batch", "SrConfig", "SrBuffers", "SrError",
     "sr_session_init", "sr_session_restore", "sr_session_frames", "sr_rope3d_qk", "sr_chunk_attention",
     "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch", "sr_device_error_status",
-    "sr_debug_wait_timeout",
+    "sr_debug_wait_timeout", "sr_workspace_bytes",
 ]
 
 _BF16 = torch.bfloat16
@@ -53,7 +53,8 @@ class Session:
     def __init__(self, n_heads: int, head_dim: int, grid_h: int, grid_w: int, chunk_frames: int,
                  window_frames: int, n_sink: int, n_steps: int = 2, *, sink_k: torch.Tensor | None = None,
                  sink_v: torch.Tensor | None = None, t_clock0: int = 0, rope_base: float = 10000.0,
-                 softmax_scale: float = 0.0, wait_timeout_ns: int = 0, device="cuda"):
+                 softmax_scale: float = 0.0, wait_timeout_ns: int = 0, tail_split: int = 0,
+                 workspace: bool = True, device="cuda"):
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
@@ -74,9 +75,14 @@ class Session:
             _check_tensor("sink_k", sink_k, self.sink_k.shape, dev)
             _check_tensor("sink_v", sink_v, self.sink_v.shape, dev)
         self.cfg = SrConfig(n_heads, head_dim, grid_h, grid_w, chunk_frames, window_frames, n_sink, n_steps,
-                            t_clock0, rope_base, softmax_scale, wait_timeout_ns)
+                            t_clock0, rope_base, softmax_scale, wait_timeout_ns, tail_split)
+        # scratch for key-split last blocks (256-byte aligned: torch's allocator aligns to 512)
+        self.workspace = None
+        if workspace:
+            nbytes = sr_workspace_bytes(self.cfg)
+            self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
         self.bufs = SrBuffers(_ptr(self.sink_k), _ptr(self.sink_v), _ptr(self.ring_k), _ptr(self.ring_v),
-                              self.slot_frame.data_ptr(), self.err_word.data_ptr())
+                              self.slot_frame.data_ptr(), self.err_word.data_ptr(), _ptr(self.workspace))
         self.handle = None
         with torch.cuda.device(dev):
             self.handle = sr_session_init(self.cfg, self.bufs, _ptr(sink_k), _ptr(sink_v), _stream(dev))

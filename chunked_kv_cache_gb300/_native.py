@@ -26,7 +26,7 @@ SR_MAX_BATCH = 16
 EXPORTS = (
     "sr_session_init", "sr_session_restore", "sr_session_frames", "sr_rope3d_qk",
     "sr_chunk_attention", "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch",
-    "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string",
+    "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string", "sr_workspace_bytes",
 )
 
 
@@ -38,6 +38,7 @@ class SrConfig(ctypes.Structure):
         ("n_sink", ctypes.c_int32), ("n_steps", ctypes.c_int32),
         ("t_clock0", ctypes.c_int32), ("rope_base", ctypes.c_float),
         ("softmax_scale", ctypes.c_float), ("wait_timeout_ns", ctypes.c_uint64),
+        ("tail_split", ctypes.c_int32),
     ]
 
 
@@ -46,6 +47,7 @@ class SrBuffers(ctypes.Structure):
         ("sink_k", ctypes.c_void_p), ("sink_v", ctypes.c_void_p),
         ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p),
         ("slot_frame", ctypes.c_void_p), ("err_word", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
     ]
 
 
@@ -79,6 +81,7 @@ def lib() -> ctypes.CDLL:
                                                ctypes.POINTER(i64), vp, vp, vp]
         L.sr_device_error_status.argtypes = [i32]
         L.sr_debug_wait_timeout.argtypes = [vp, u64, vp]
+        L.sr_workspace_bytes.argtypes = [ctypes.POINTER(SrConfig), ctypes.POINTER(ctypes.c_uint64)]
         L.sr_status_string.argtypes = [ctypes.c_int]
         L.sr_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -102,6 +105,12 @@ def sr_session_init(cfg: SrConfig, bufs: SrBuffers, sink_k_src: int, sink_v_src:
     _check(lib().sr_session_init(ctypes.byref(cfg), ctypes.byref(bufs), sink_k_src or None,
                                  sink_v_src or None, stream or None, ctypes.byref(out)), "sr_session_init")
     return out.value
+
+
+def sr_workspace_bytes(cfg: SrConfig) -> int:
+    n = ctypes.c_uint64()
+    _check(lib().sr_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "sr_workspace_bytes")
+    return n.value
 
 
 def sr_session_restore(handle: int, n_committed: int) -> None:

@@ -88,6 +88,7 @@ struct SmemBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int last;       // key-split last block: this CTA is the last part and merges
   float xm[BM];   // split mode: group 1's running max / sum, handed to group 0
   float xl[BM];
 };
@@ -104,13 +105,14 @@ struct TileMap {
   }
 };
 
-// The key tiles each query tile walks: in shared mode both walk all n tiles;
-// in split mode tile 0 walks [0, h) and tile 1 walks [h, n).
+// The key tiles each query tile walks, within the unit's range [lo, lo + n) of
+// all key tiles: in shared mode both walk the whole range; in split mode tile 0
+// walks [lo, lo + h) and tile 1 walks [lo + h, lo + n).
 struct Walk {
   bool split;
-  int n, h;
+  int lo, n, h;
   __device__ __forceinline__ int count(int t) const { return split ? (t == 0 ? h : n - h) : n; }
-  __device__ __forceinline__ int kv(int t, int i) const { return (split && t == 1) ? h + i : i; }
+  __device__ __forceinline__ int kv(int t, int i) const { return lo + ((split && t == 1) ? h + i : i); }
   __device__ __forceinline__ int iters() const { return split ? h : n; }
 };
 
@@ -120,7 +122,8 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 
 template <int NSESS>
 __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, int H, int& si, int& head,
-                                            int& qb) {
+                                            int& qb, int& part) {
+  part = 0;
   if (u < p.n_full_units) {
     si = 0;
 #pragma unroll 1
@@ -130,9 +133,12 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
     head = local / nf;
     qb = local % nf;
   } else {
+    // every session has H last blocks, each run as tail_split key-range parts
     const int t = u - p.n_full_units;
-    si = t / H;                       // every session has exactly H last-block units
-    head = t - si * H;
+    const int tail = t / p.tail_split;
+    part = t - tail * p.tail_split;
+    si = tail / H;
+    head = tail - si * H;
     qb = p.sess[si].nqb - 1;
   }
 }
@@ -149,16 +155,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  int si, head, qb;
-  decode_unit(p, static_cast<int>(blockIdx.x), p.n_heads, si, head, qb);
+  int si, head, qb, part;
+  decode_unit(p, static_cast<int>(blockIdx.x), p.n_heads, si, head, qb, part);
   const AttnSession& S = p.sess[si];
   const int q_local0 = qb * 2 * BM;                       // first query row of the unit (session-local)
   const int n_qtiles = min(2, (S.lq - q_local0 + BM - 1) / BM);
   TileMap tm;
 #pragma unroll
   for (int s = 0; s < 3; ++s) tm.nt[s] = (S.seg_rows[s] + BN - 1) / BN;
-  const int n_kv = tm.nt[0] + tm.nt[1] + tm.nt[2];
-  const Walk wk{n_qtiles == 1, n_kv, n_qtiles == 1 ? (n_kv + 1) / 2 : n_kv};
+  const int n_kv_all = tm.nt[0] + tm.nt[1] + tm.nt[2];
+  // a single-tile last block may be one of `parts` CTAs sharing its key range
+  const int parts = (n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
+  const int kv_lo = static_cast<int>(static_cast<int64_t>(part) * n_kv_all / parts);
+  const int n_kv = static_cast<int>(static_cast<int64_t>(part + 1) * n_kv_all / parts) - kv_lo;
+  const Walk wk{n_qtiles == 1, kv_lo, n_kv, n_qtiles == 1 ? (n_kv + 1) / 2 : n_kv};
 
   WaitCtx wc{&bars->abort, p.err_word, p.timeout_ns};
 
@@ -450,6 +460,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       f0 *= inv_l;
       f1 *= inv_l;
       __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
+      // one part of a key-split last block publishes fp32 rows and their log2-sum-exp
+      float* pdst = parts > 1 ? S.ws_part + ((static_cast<int64_t>(head) * kMaxTailSplit + part) * BM + row) * (D + 4)
+                              : nullptr;
       const uint32_t t_o1 = tmem + lane_base + 256 + 128;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -470,17 +483,85 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f0);
         }
         if (live) {
-          uint4 pkt[4];
-          uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
+          if (pdst) {
+            float4* d4 = reinterpret_cast<float4*>(pdst + c * 32);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                  __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          } else {
+            uint4 pkt[4];
+            uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = pkt[i];
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = pkt[i];
+          }
         }
       }
-      if (live && p.lse != nullptr)
-        p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = (m + __log2f(l)) * 0.69314718055994531f;
+      if (live) {
+        const float lse2 = m + __log2f(l);
+        if (pdst)
+          pdst[D] = lse2;
+        else if (p.lse != nullptr)
+          p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = lse2 * 0.69314718055994531f;
+      }
+    }
+    if (writer && parts > 1) {
+      // Every part has published its rows; the last part to arrive merges them.
+      // The counter holds (epoch << 4 | arrivals): raising it to this call's
+      // epoch first discards any count left by an earlier, aborted call.
+      __threadfence();
+      named_sync(2, BM);
+      if (threadIdx.x == 0) {
+        int last = 0;
+        if (ok) {
+          int* ctr = S.ws_ctr + head;
+          atomicMax(ctr, S.epoch << 4);
+          const int old = atomicAdd(ctr, 1);
+          last = ((old >> 4) == S.epoch) && ((old & 15) == parts - 1);
+        }
+        bars->last = last;
+      }
+      named_sync(2, BM);
+      if (bars->last && live) {
+        __threadfence();
+        const float* base = S.ws_part + (static_cast<int64_t>(head) * kMaxTailSplit * BM + row) * (D + 4);
+        const int64_t pstride = static_cast<int64_t>(BM) * (D + 4);
+        float w[kMaxTailSplit];
+        float mx = -INFINITY;
+        for (int k = 0; k < parts; ++k) {
+          w[k] = __ldcg(base + k * pstride + D);
+          mx = fmaxf(mx, w[k]);
+        }
+        float L = 0.f;
+        for (int k = 0; k < parts; ++k) {
+          w[k] = ex2_approx(w[k] - mx);
+          L += w[k];
+        }
+        const float invL = 1.f / L;
+        for (int k = 0; k < parts; ++k) w[k] *= invL;
+        __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 8) {
+          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int k = 0; k < parts; ++k) {
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c));
+            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c + 4));
+            a[0] += w[k] * x0.x; a[1] += w[k] * x0.y; a[2] += w[k] * x0.z; a[3] += w[k] * x0.w;
+            a[4] += w[k] * x1.x; a[5] += w[k] * x1.y; a[6] += w[k] * x1.z; a[7] += w[k] * x1.w;
+          }
+          uint4 pkt;
+          pkt.x = pack_bf16x2(a[0], a[1]);
+          pkt.y = pack_bf16x2(a[2], a[3]);
+          pkt.z = pack_bf16x2(a[4], a[5]);
+          pkt.w = pack_bf16x2(a[6], a[7]);
+          *reinterpret_cast<uint4*>(dst + c) = pkt;
+        }
+        if (p.lse != nullptr)
+          p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = (mx + __log2f(L)) * 0.69314718055994531f;
+      }
     }
   }
 

@@ -158,8 +158,10 @@ __global__ void copy16_kernel(uint4* __restrict__ dst, const uint4* __restrict__
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     dst[i] = src[i];
 }
-__global__ void init_ring_state_kernel(int32_t* slot_frame, int W, int32_t* err_word) {
+__global__ void init_ring_state_kernel(int32_t* slot_frame, int W, int32_t* err_word, int32_t* ws_ctr, int n_ctr) {
   for (int i = threadIdx.x; i < W; i += blockDim.x) slot_frame[i] = -1;
+  if (ws_ctr)
+    for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ws_ctr[i] = 0;
   if (threadIdx.x == 0) *err_word = SR_DEVERR_NONE;
 }
 }  // namespace
@@ -173,8 +175,9 @@ cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, cudaStream_t st) {
-  init_ring_state_kernel<<<1, 256, 0, st>>>(slot_frame, W, err_word);
+cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, int32_t* ws_ctr, int n_ctr,
+                                   cudaStream_t st) {
+  init_ring_state_kernel<<<1, 256, 0, st>>>(slot_frame, W, err_word, ws_ctr, n_ctr);
   return cudaGetLastError();
 }
 

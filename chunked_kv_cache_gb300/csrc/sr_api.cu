@@ -19,8 +19,11 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <new>
+#include <queue>
+#include <vector>
 
 #include "sr.h"
 #include "sr_kernels.h"
@@ -32,6 +35,7 @@ struct sr_session {
   int64_t lq;                 // F*T
   float scale;
   int64_t n_committed;
+  int32_t epoch;              // attention calls so far (key-split counters)
   double inv_freq[64];
   int8_t axis[64];
 };
@@ -52,6 +56,7 @@ sr_status validate_config(const sr_config& c) {
   if (c.window_frames > 0 && c.window_frames < c.chunk_frames) return SR_ERR_INVALID_ARG;
   if (!(c.rope_base > 1.0f) || !std::isfinite(c.rope_base)) return SR_ERR_INVALID_ARG;
   if (!std::isfinite(c.softmax_scale)) return SR_ERR_INVALID_ARG;
+  if (c.tail_split < 0 || c.tail_split > SR_MAX_TAIL_SPLIT) return SR_ERR_INVALID_ARG;
   // every element offset must fit comfortably in 32-bit row counts
   const int64_t row = static_cast<int64_t>(c.n_heads) * c.head_dim;
   const int64_t T = static_cast<int64_t>(c.grid_h) * c.grid_w;
@@ -137,7 +142,7 @@ cudaError_t ensure_attn_attr(int head_dim, int nsess_template) {
 
 // Fill one session's segment maps for `step` (rows of the chunk taken from
 // k, v at row offset `row0` of a packed tensor).
-sr_status fill_session(sr::AttnSession& out, const sr_session* s, int step, const void* k, const void* v,
+sr_status fill_session(sr::AttnSession& out, sr_session* s, int step, const void* k, const void* v,
                        int64_t row0) {
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
   const int64_t S = s->cfg.n_sink;
@@ -166,7 +171,88 @@ sr_status fill_session(sr::AttnSession& out, const sr_session* s, int step, cons
   out.q_row0 = static_cast<int32_t>(row0);
   out.lq = static_cast<int32_t>(s->lq);
   out.nqb = static_cast<int32_t>((s->lq + 255) / 256);
+  if (s->buf.workspace) {
+    char* ws = static_cast<char*>(s->buf.workspace);
+    out.ws_ctr = reinterpret_cast<int32_t*>(ws);
+    out.ws_part = reinterpret_cast<float*>(ws + sr::ws_counter_bytes(s->cfg.n_heads));
+    s->epoch = (s->epoch + 1) & 0x07FFFFFF;
+    if (s->epoch == 0) s->epoch = 1;
+    out.epoch = s->epoch;
+  }
   return SR_OK;
+}
+
+int sm_count() {
+  static int counts[64];
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return 148;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+// Key tiles a session's chunk attends over (sink bank + occupied ring + chunk).
+int64_t key_tiles(const sr_session* s) {
+  const int64_t rows[3] = {s->cfg.n_sink,
+                           std::min<int64_t>(s->n_committed, s->cfg.window_frames) * s->tokens_per_frame, s->lq};
+  int64_t n = 0;
+  for (int64_t r : rows) n += (r + 127) / 128;
+  return n;
+}
+
+// How many CTAs share the key range of each single-tile last block. Units are
+// dispatched in order (full blocks, then last blocks) to whichever SM frees up
+// first, one CTA per SM; estimate that schedule's makespan for 1..4 parts and
+// keep the best. Cost model in key-tile iterations: a full block walks all its
+// key tiles with two query tiles; a last-block part walks its share split over
+// two halves, about 1.35x slower per iteration (two K/V streams), plus a small
+// merge charge.
+int choose_tail_split(sr_session* const* ss, const int* order, int n) {
+  int forced = ss[0]->cfg.tail_split;
+  int64_t min_kv = INT64_MAX;
+  for (int r = 0; r < n; ++r) {
+    const sr_session* s = ss[order[r]];
+    const int64_t rem = s->lq % 256;
+    if (!s->buf.workspace || rem == 0 || rem > 128) return 1;   // no single-tile last block
+    min_kv = std::min(min_kv, key_tiles(s));
+  }
+  const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, min_kv));
+  if (forced > 0) return std::max(1, std::min(forced, cap));
+  const int G = sm_count();
+  int best = 1;
+  double best_t = 0;
+  for (int k = 1; k <= cap; ++k) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int g = 0; g < G; ++g) free_at.push(0.0);
+    auto run = [&](double cost) {
+      const double t0 = free_at.top();
+      free_at.pop();
+      free_at.push(t0 + cost);
+    };
+    for (int r = 0; r < n; ++r) {
+      const sr_session* s = ss[order[r]];
+      const int64_t units = static_cast<int64_t>(s->cfg.n_heads) * ((s->lq + 255) / 256 - 1);
+      for (int64_t u = 0; u < units; ++u) run(static_cast<double>(key_tiles(s)));
+    }
+    for (int r = 0; r < n; ++r) {
+      const sr_session* s = ss[order[r]];
+      const double part = std::ceil(std::ceil(static_cast<double>(key_tiles(s)) / k) / 2.0) * 1.35 + (k > 1 ? 2.0 : 0.0);
+      for (int64_t u = 0; u < static_cast<int64_t>(s->cfg.n_heads) * k; ++u) run(part);
+    }
+    double t = 0;
+    while (!free_at.empty()) {
+      t = std::max(t, free_at.top());
+      free_at.pop();
+    }
+    if (k == 1 || t < best_t * 0.98) {
+      best = k;
+      best_t = t;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -188,6 +274,15 @@ const char* sr_status_string(sr_status st) {
 
 sr_status sr_device_error_status(int32_t v) { return v == SR_DEVERR_NONE ? SR_OK : SR_ERR_TIMEOUT; }
 
+sr_status sr_workspace_bytes(const sr_config* cfg, uint64_t* bytes) {
+  if (!cfg || !bytes) return SR_ERR_INVALID_ARG;
+  sr_status st = validate_config(*cfg);
+  if (st != SR_OK) return st;
+  *bytes = sr::ws_counter_bytes(cfg->n_heads) +
+           static_cast<uint64_t>(cfg->n_heads) * sr::ws_partial_floats_per_head(cfg->head_dim) * sizeof(float);
+  return SR_OK;
+}
+
 sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const void* sink_k_src,
                           const void* sink_v_src, void* stream, sr_session** out) {
   if (out) *out = nullptr;
@@ -204,6 +299,7 @@ sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const vo
       (has_ring && (!aligned16(bufs->ring_k) || !aligned16(bufs->ring_v))) ||
       (sink_k_src && (!aligned16(sink_k_src) || !aligned16(sink_v_src))) ||
       (reinterpret_cast<uintptr_t>(bufs->err_word) & 3u) ||
+      (reinterpret_cast<uintptr_t>(bufs->workspace) & 255u) ||
       (reinterpret_cast<uintptr_t>(bufs->slot_frame) & 3u))
     return SR_ERR_ALIGN;
 
@@ -226,7 +322,9 @@ sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const vo
     e = sr::launch_copy16(bufs->sink_k, sink_k_src, bytes, cs);
     if (e == cudaSuccess) e = sr::launch_copy16(bufs->sink_v, sink_v_src, bytes, cs);
   }
-  if (e == cudaSuccess) e = sr::launch_init_ring_state(bufs->slot_frame, cfg->window_frames, bufs->err_word, cs);
+  if (e == cudaSuccess)
+    e = sr::launch_init_ring_state(bufs->slot_frame, cfg->window_frames, bufs->err_word,
+                                   static_cast<int32_t*>(bufs->workspace), cfg->n_heads, cs);
   if (e == cudaSuccess) e = ensure_attn_attr(cfg->head_dim, 1);
   if (e == cudaSuccess) e = ensure_attn_attr(cfg->head_dim, sr::kAttnMaxBatch);
   if (e != cudaSuccess) {
@@ -320,7 +418,9 @@ sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const v
     p->sess[0].unit_begin = 0;
     p->sess[0].tail_begin = 0;
     p->n_full_units = s->cfg.n_heads * (p->sess[0].nqb - 1);
-    n_units = s->cfg.n_heads * p->sess[0].nqb;
+    const int order0 = 0;
+    p->tail_split = choose_tail_split(&s, &order0, 1);
+    n_units = p->n_full_units + s->cfg.n_heads * p->tail_split;
     p->n_sess = 1;
     p->n_heads = s->cfg.n_heads;
     p->scale_log2 = s->scale * 1.4426950408889634f;
@@ -381,9 +481,11 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
     full += s0->cfg.n_heads * (p->sess[r].nqb - 1);
     tails += s0->cfg.n_heads;
   }
-  const int units = full + tails;
+  const int split = st == SR_OK ? choose_tail_split(sessions, order, n) : 1;
+  const int units = full + tails * split;
   if (st == SR_OK) {
     p->n_full_units = full;
+    p->tail_split = split;
     p->n_sess = n;
     p->n_heads = s0->cfg.n_heads;
     p->scale_log2 = s0->scale * 1.4426950408889634f;

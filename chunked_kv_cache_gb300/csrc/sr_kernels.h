@@ -25,6 +25,9 @@ struct alignas(128) AttnSession {
   int32_t nqb;          // query blocks of 256 rows
   int32_t unit_begin;   // first full-block unit of this session (full blocks come first)
   int32_t tail_begin;   // index of this session's last-block units among all last-block units
+  float* ws_part;       // key-split partials: [H][kMaxTailSplit][128][d + 4] fp32 (NULL: no split)
+  int32_t* ws_ctr;      // [H] per-head arrival counters (epoch << 4 | count)
+  int32_t epoch;        // this call's epoch for the counters (increases per call of the session)
 };
 
 template <int NSESS>
@@ -33,6 +36,7 @@ struct alignas(128) AttnParams {
   AttnSession sess[NSESS];
   int32_t n_sess;
   int32_t n_full_units;           // units of full 256-row blocks (all sessions); last blocks follow
+  int32_t tail_split;             // CTAs per last block (1: no key split)
   int32_t n_heads;
   float scale_log2;               // softmax scale * log2(e)
   int32_t lse_ld;                 // row stride of lse ([H][lse_ld]); 0 when lse is NULL
@@ -75,7 +79,13 @@ cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st);
 
 // ------------------------------------------------------------ misc
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);
-cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, cudaStream_t st);
+cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, int32_t* ws_ctr, int n_ctr,
+                                   cudaStream_t st);
+
+constexpr int kMaxTailSplit = SR_MAX_TAIL_SPLIT;
+// workspace layout: counters (padded to 256 B), then the partials
+inline size_t ws_counter_bytes(int n_heads) { return (static_cast<size_t>(n_heads) * 4 + 255) / 256 * 256; }
+inline size_t ws_partial_floats_per_head(int head_dim) { return static_cast<size_t>(kMaxTailSplit) * 128 * (head_dim + 4); }
 cudaError_t launch_debug_wait(int32_t* err_word, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace sr

@@ -79,6 +79,9 @@ typedef struct {
   float rope_base;          /* rotary base (e.g. 10000); > 1 */
   float softmax_scale;      /* <= 0 selects 1/sqrt(head_dim) */
   uint64_t wait_timeout_ns; /* bound on every device-side wait; 0 selects 2 s */
+  int32_t tail_split;       /* key-range split of a chunk's last, single-tile query block across
+                               CTAs: 0 = chosen per call, 1 = never, 2..4 = exactly that many
+                               (needs a workspace; clamped to the number of key tiles) */
 } sr_config;
 
 /* Caller-owned device buffers of one session (all 16-byte aligned). */
@@ -89,7 +92,18 @@ typedef struct {
   void* ring_v;             /* [W*T][H][d] bf16 */
   int32_t* slot_frame;      /* [W] int32: absolute frame held by each slot, -1 = empty */
   int32_t* err_word;        /* [1] int32: device error word (see SR_DEVERR_*) */
+  void* workspace;          /* optional, 256-byte aligned, sr_workspace_bytes() long: partial
+                               results of key-split last blocks. NULL disables the split. The
+                               library initialises it in sr_session_init; do not modify it after. */
 } sr_buffers;
+
+#define SR_MAX_TAIL_SPLIT 4
+
+/*
+ * Bytes of workspace a session with this config can use (see sr_buffers.workspace):
+ * per head, SR_MAX_TAIL_SPLIT partial results of 128 rows plus a counter.
+ */
+SR_API sr_status sr_workspace_bytes(const sr_config* cfg, uint64_t* bytes);
 
 /*
  * Create a session. Copies the sink banks from sink_k_src / sink_v_src (device,
@@ -134,6 +148,10 @@ SR_API sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream);
  * q, k, v: [F*T][H][d] bf16 (q and k already rotated); o: [F*T][H][d] bf16 output.
  * lse: optional [H][F*T] fp32 natural-log sum-exp of the scaled scores (NULL to skip).
  * bf16 operands, fp32 accumulation and fp32 online softmax on the tensor cores.
+ * When the chunk's last 256-row query block holds a single 128-row tile and the
+ * session has a workspace, that block's key range may be split over several CTAs
+ * (sr_config.tail_split); the last CTA to finish merges the partial results. Calls
+ * of one session that overlap on the GPU race on that workspace.
  */
 SR_API sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const void* k,
                              const void* v, void* o, float* lse, void* stream);

@@ -69,7 +69,8 @@ class Twin:
     """A CUDA session and an oracle session in the same state."""
 
     def __init__(self, shape: syn.Shape, config: int, fill: int = 0, session: int = 0, t_clock0: int = 0,
-                 n_sink=None, window_frames=None, dev=None, heads=None):
+                 n_sink=None, window_frames=None, dev=None, heads=None, tail_split: int = 0,
+                 workspace: bool = True):
         import chunked_kv_cache_gb300 as sr
         self.dev = dev or device()
         self.shape = shape
@@ -81,7 +82,7 @@ class Twin:
         sk, sv = syn.session_sinks(sh, config, session)
         self.gpu = sr.Session(sh.n_heads, sh.head_dim, sh.grid_h, sh.grid_w, sh.chunk_frames, W, S, sh.n_steps,
                               sink_k=to_dev(sk, self.dev), sink_v=to_dev(sv, self.dev), t_clock0=t_clock0,
-                              device=self.dev)
+                              tail_split=tail_split, workspace=workspace, device=self.dev)
         # the oracle may follow only a subset of heads (heads are independent)
         self.heads = None if heads is None else np.asarray(heads)
         hs = slice(None) if heads is None else self.heads

@@ -126,3 +126,21 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(N, "LIB_PATH", str(tmp_path / "libsr.so"))
     with pytest.raises(OSError, match="no fallback"):
         N.lib()
+
+
+def test_workspace_bytes_closed_form(lib):
+    n = N.sr_workspace_bytes(_cfg(n_heads=24, head_dim=128))
+    # counters (24 x 4 B, padded to 256) + 24 heads x 4 parts x 128 rows x (128 + 4) floats
+    assert n == 256 + 24 * 4 * 128 * 132 * 4
+    assert N.sr_workspace_bytes(_cfg(n_heads=100, head_dim=64)) == 512 + 100 * 4 * 128 * 68 * 4
+
+
+@pytest.mark.parametrize("value", [-1, 5])
+def test_tail_split_out_of_range(lib, value):
+    st, out = _init(_cfg(tail_split=value), _bufs())
+    assert st == N.SR_ERR_INVALID_ARG and out is None
+
+
+def test_misaligned_workspace(lib):
+    st, out = _init(_cfg(), _bufs(workspace=0x70080))
+    assert st == N.SR_ERR_ALIGN and out is None

@@ -184,12 +184,49 @@ def test_clock_shift_invariance_without_sinks():
     assert np.abs(outs[0] - outs[1]).max() <= 2e-2 and np.abs(outs[0] - outs[2]).max() <= 2e-2
 
 
+# ------------------------------------------------------------------ key-split last blocks
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+def test_key_split_last_block_832x480(k):
+    # rows 3072..3119 form a single-tile last block per head; its key range is
+    # spread over k CTAs whose partial results the last one merges
+    shape = syn.SHAPE_832x480
+    tw = Twin(shape, 2, fill=6, heads=[1, 22], tail_split=k)
+    x = syn.chunk_inputs(shape, 2, chunk=11)
+    rows = sorted(set(list(range(3072, 3120)) + [0, 255, 3071]))
+    for rep in range(2):      # a second call exercises the next epoch of the arrival counters
+        got, ref, gl, rl = tw.step(x, 0, rows=rows, lse=True)
+        assert_attention_close(got, ref, f"key split {k}, call {rep}")
+        assert np.abs(gl - rl).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_key_split_tiny_all_units_split(k):
+    # Lq = 120: every unit is a single-tile block; with 4 key tiles and k = 4 each
+    # part walks one tile and its second softmax group has nothing to do
+    shape = syn.TINY
+    tw = Twin(shape, 1, fill=4, tail_split=k)
+    x = syn.chunk_inputs(shape, 1, chunk=2)
+    got, ref, gl, rl = tw.step(x, 1, lse=True)
+    assert_attention_close(got, ref, f"tiny key split {k}")
+    assert np.abs(gl - rl).max() <= LSE_ABS
+
+
+def test_key_split_needs_workspace():
+    # without a workspace the split is off and results still match
+    shape = syn.TINY
+    tw = Twin(shape, 1, fill=2, tail_split=4, workspace=False)
+    got, ref, _, _ = tw.step(syn.chunk_inputs(shape, 1, chunk=3), 0)
+    assert_attention_close(got, ref, "no workspace")
+
+
 # ------------------------------------------------------------------ multi-session batch
 
 def test_batch_matches_single_and_oracle():
     import chunked_kv_cache_gb300 as sr
     shape = syn.SHAPE_832x480
-    twins = [Twin(shape, 5, fill=f, session=i, heads=[0, 13]) for i, f in enumerate(syn.BATCH_FILLS)]
+    # a fixed key split of the last blocks, so that batch and single calls run the same parts
+    twins = [Twin(shape, 5, fill=f, session=i, heads=[0, 13], tail_split=2) for i, f in enumerate(syn.BATCH_FILLS)]
     xs = [syn.chunk_inputs(shape, 5, session=i) for i in range(len(twins))]
     dev = twins[0].dev
     step = 1
