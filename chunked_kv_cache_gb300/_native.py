@@ -27,6 +27,7 @@ EXPORTS = (
     "sr_session_init", "sr_session_restore", "sr_session_frames", "sr_rope3d_qk",
     "sr_chunk_attention", "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch",
     "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string", "sr_workspace_bytes",
+    "sr_chunk_attention_noalloc",
 )
 
 
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
         L.sr_rope3d_qk.argtypes = [vp, vp, vp, vp]
         L.sr_chunk_attention.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
         L.sr_cache_commit.argtypes = [vp, vp, vp, vp]
+        L.sr_chunk_attention_noalloc.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
         L.sr_session_free.argtypes = [vp]
         L.sr_chunk_attention_batch.argtypes = [ctypes.POINTER(vp), i32, i32, vp, vp, vp,
                                                ctypes.POINTER(i64), vp, vp, vp]
@@ -130,6 +132,14 @@ def sr_rope3d_qk(handle: int, q: int, k: int, stream: int) -> None:
 def sr_chunk_attention(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int, stream: int) -> None:
     _check(lib().sr_chunk_attention(handle, int(step), q, k, v, o, lse or None, stream or None),
            "sr_chunk_attention")
+
+
+def sr_chunk_attention_noalloc(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int,
+                               stream: int) -> None:
+    """sr_chunk_attention with the library's built-in scratch instead of a workspace,
+    for callers that cannot allocate device memory."""
+    _check(lib().sr_chunk_attention_noalloc(handle, int(step), q, k, v, o, lse or None, stream or None),
+           "sr_chunk_attention_noalloc")
 
 
 def sr_cache_commit(handle: int, k_raw: int, v: int, stream: int) -> None:

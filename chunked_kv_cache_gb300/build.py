@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsr.so")
-SOURCES = ["attention.cu", "rope_commit.cu", "sr_api.cu"]
+SOURCES = ["attention.cu", "rope_commit.cu", "sr_api.cu", "sr_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

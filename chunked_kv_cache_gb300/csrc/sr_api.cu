@@ -257,6 +257,56 @@ int choose_tail_split(sr_session* const* ss, const int* order, int n) {
 
 }  // namespace
 
+// ------------------------------------------------------------ allocation-free path
+namespace sr {
+
+int session_heads(const sr_session* s) { return s->cfg.n_heads; }
+
+sr_status attention_scratch_check(const sr_session* s, int32_t step, const void* q, const void* k, const void* v,
+                                  const void* o, const float* lse, uint64_t scratch_bytes) {
+  if (!s || !q || !k || !v || !o) return SR_ERR_INVALID_ARG;
+  if (step < 0 || step >= s->cfg.n_steps) return SR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return SR_ERR_ALIGN;
+  uint64_t need = 0;
+  if (sr_workspace_bytes(&s->cfg, &need) != SR_OK || need > scratch_bytes) return SR_ERR_UNSUPPORTED;
+  return SR_OK;
+}
+
+sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, const void* k, const void* v, void* o,
+                                 float* lse, void* stream, void* scratch) {
+  if (ensure_attn_attr(s->cfg.head_dim, 1) != cudaSuccess) return SR_ERR_CUDA;
+  AttnParams<1> p;                                  // on the stack: nothing is allocated
+  std::memset(&p, 0, sizeof(p));
+  const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
+  if (!encode_rows(&p.qmap, q, s->lq, row_elems)) return SR_ERR_CUDA;
+  // the scratch stands in for the session's workspace for this call only
+  void* own = s->buf.workspace;
+  s->buf.workspace = scratch;
+  sr_status st = fill_session(p.sess[0], s, step, k, v, 0);
+  const int order0 = 0;
+  const int split = st == SR_OK ? choose_tail_split(&s, &order0, 1) : 1;
+  s->buf.workspace = own;
+  if (st != SR_OK) return st;
+  p.n_full_units = s->cfg.n_heads * (p.sess[0].nqb - 1);
+  p.tail_split = split;
+  const int n_units = p.n_full_units + s->cfg.n_heads * split;
+  p.n_sess = 1;
+  p.n_heads = s->cfg.n_heads;
+  p.scale_log2 = s->scale * 1.4426950408889634f;
+  p.lse_ld = lse ? static_cast<int32_t>(s->lq) : 0;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.err_word = s->buf.err_word;
+  p.timeout_ns = s->cfg.wait_timeout_ns;
+  return launch_attention_1(p, s->cfg.head_dim, n_units, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SR_OK
+             : SR_ERR_CUDA;
+}
+
+}  // namespace sr
+
 extern "C" {
 
 const char* sr_status_string(sr_status st) {

@@ -83,6 +83,16 @@ cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word
                                    cudaStream_t st);
 
 constexpr int kMaxTailSplit = SR_MAX_TAIL_SPLIT;
+
+// Used only by the allocation-free entry point (sr_noalloc.cu): validate a
+// chunk-attention call against a scratch area of scratch_bytes (no side
+// effects), then launch it with that scratch standing in for the session's
+// workspace. Neither allocates anything.
+sr_status attention_scratch_check(const sr_session* s, int32_t step, const void* q, const void* k, const void* v,
+                                  const void* o, const float* lse, uint64_t scratch_bytes);
+sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, const void* k, const void* v, void* o,
+                                 float* lse, void* stream, void* scratch);
+int session_heads(const sr_session* s);
 // workspace layout: counters (padded to 256 B), then the partials
 inline size_t ws_counter_bytes(int n_heads) { return (static_cast<size_t>(n_heads) * 4 + 255) / 256 * 256; }
 inline size_t ws_partial_floats_per_head(int head_dim) { return static_cast<size_t>(kMaxTailSplit) * 128 * (head_dim + 4); }

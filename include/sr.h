@@ -184,6 +184,29 @@ SR_API sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n
                                    const void* q, const void* k, const void* v,
                                    const int64_t* q_off, void* o, float* lse, void* stream);
 
+/*
+ * sr_chunk_attention for callers that cannot allocate device memory. (The pages
+ * have no counterpart: this is a deployment convenience of this library.)
+ * Some callers cannot call cudaMalloc or hand over a workspace: code running inside
+ * a framework's fixed memory pool, a plugin that must not touch the allocator, or a
+ * process that only receives a stream and its tensors. This entry point computes
+ * exactly what sr_chunk_attention computes, with the same arguments, but the scratch
+ * of key-split last blocks comes from a 16 MiB array compiled into the library
+ * (held on every GPU that loads it until the process exits) instead of the
+ * session's workspace, which may be NULL. It allocates nothing.
+ * - Limit: sessions whose sr_workspace_bytes() exceeds 16 MiB (for example more
+ *   than 62 heads at head_dim 128) are rejected with SR_ERR_UNSUPPORTED before
+ *   anything is launched.
+ * - The first call on a device does one-time set-up (it looks up the array's device
+ *   address and sets the kernel's shared-memory limit); make that first call before
+ *   any stream capture.
+ * - Every call shares the one array: the counters that must start at zero are
+ *   cleared on the stream before each launch, and calls that overlap on the GPU
+ *   (other streams, other threads, other sessions) race on it.
+ */
+SR_API sr_status sr_chunk_attention_noalloc(sr_session* s, int32_t step, const void* q, const void* k,
+                                            const void* v, void* o, float* lse, void* stream);
+
 /* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
 SR_API sr_status sr_device_error_status(int32_t err_word_value);
 
