@@ -231,8 +231,11 @@ def run_ours(args):
     attn_avg = statistics.mean(attn_ms)
     achieved = flops_attn / (attn_avg / 1e3) / 1e12
     value = aggregate_throughput(args.steps * flops_chunk, elapsed, world) / 1e12
-    commit_avg = statistics.mean(commit_ms)
-    rope_avg = statistics.mean(rope_ms)
+    # The two HBM-bound kernels last ~20 us, close to the event timer's
+    # granularity; time them again over 16 back-to-back launches each, cycling
+    # through six input pairs of the two sessions (230 MB at 832x480, more than
+    # the L2) so the inputs of a launch are not in L2.
+    rope_avg, commit_avg = hbm_kernel_times(sessions, shape)
     cpu = cpu_baseline(shape, args) if world == 1 and not args.profile else None
     traffic = _profiled_traffic("chunk_attention", args.config)
     out = {
@@ -267,6 +270,30 @@ def run_ours(args):
     print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def hbm_kernel_times(sessions, shape, reps: int = 16):
+    """Mean ms per launch of RoPE-3D (mode 0) and of the ring commit, each timed
+    over `reps` back-to-back launches between one pair of events."""
+    pairs = [(x["q"][st], x["k"][st]) for _, x in sessions for st in range(shape.n_steps)]
+    pairs += [(x["clean_k"], x["clean_v"]) for _, x in sessions]
+    out = []
+    for kind in ("rope", "commit"):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record()
+        for i in range(reps):
+            if kind == "rope":
+                s = sessions[i % len(sessions)][0]
+                q, k = pairs[i % len(pairs)]
+                s.rope3d_qk(q, k)
+            else:
+                s, x = sessions[i % len(sessions)]
+                s.cache_commit(x["clean_k"], x["clean_v"])
+        ev1.record()
+        torch.cuda.synchronize()
+        out.append(ev0.elapsed_time(ev1) / reps)
+    return out[0], out[1]
 
 
 def run_e2e(shape, args, dev, sess):

@@ -55,9 +55,24 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) 
     p.slot_frame[g % p.window_frames] = static_cast<int32_t>(g);
   }
 
-  // Angles are formed in double and reduced to [-pi, pi] before the fp32
-  // sincos: an fp32 product pos * inv_freq alone would carry an absolute
-  // error proportional to the angle (1e-4 rad at t ~ 1000).
+  // Loads first: they are in flight while the sin/cos table is built.
+  uint4 a[kRopeVecPerThread], b[kRopeVecPerThread];
+  const uint4* s0 = reinterpret_cast<const uint4*>(p.src0);
+  const uint4* s1 = reinterpret_cast<const uint4*>(p.src1);
+#pragma unroll
+  for (int k = 0; k < kRopeVecPerThread; ++k) {
+    const int64_t v = v0 + threadIdx.x + k * kRopeThreads;
+    if (v < v1) {
+      a[k] = s0[v];
+      b[k] = s1[v];
+    }
+  }
+
+  // Angle = pos * inv_freq, carried as an unevaluated sum of two floats (the
+  // rounded product, its exact FMA error, and pos times the low half of
+  // inv_freq), then reduced by 2*pi written as two floats (Cody-Waite) before
+  // the fp32 sincos. A plain fp32 product would carry an absolute error
+  // proportional to the angle (1e-4 rad at t ~ 1000); this keeps it ~1e-7.
   for (int i = threadIdx.x; i < ntok * kPairs; i += kRopeThreads) {
     const int tok = tok_lo + i / kPairs;
     const int pr = i % kPairs;
@@ -70,29 +85,20 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) 
       pos = in_frame / p.grid_w;
     else
       pos = in_frame % p.grid_w;
-    const double ang = static_cast<double>(pos) * p.inv_freq[pr];
-    // Cody-Waite reduction by 2*pi taken as the double nearest 2*pi plus its
-    // remainder; the fma keeps k * head exact before the subtraction
-    const double k = rint(ang * 0.15915494309189535);
-    double r = fma(-k, 6.2831853071795862, ang);
-    r = fma(-k, 2.4492935982947064e-16, r);
-    float s, c;
-    sincosf(static_cast<float>(r), &s, &c);
-    cs_table[i] = make_float2(c, s);
+    const float fp = static_cast<float>(pos);            // exact below 2^24
+    const float hi = p.inv_freq_hi[pr];
+    const float prod = fp * hi;
+    const float err = fmaf(fp, p.inv_freq_lo[pr], fmaf(fp, hi, -prod));
+    const float k = rintf(prod * 0.159154943091895336f);
+    float r = fmaf(-k, 6.28318548202514648f, prod);       // 2*pi rounded to float
+    r = fmaf(-k, -1.74845553146951906e-7f, r);            // 2*pi minus that float
+    r += err;
+    float sn, cs;
+    sincosf(r, &sn, &cs);
+    cs_table[i] = make_float2(cs, sn);
   }
   __syncthreads();
 
-  uint4 a[kRopeVecPerThread], b[kRopeVecPerThread];
-  const uint4* s0 = reinterpret_cast<const uint4*>(p.src0);
-  const uint4* s1 = reinterpret_cast<const uint4*>(p.src1);
-#pragma unroll
-  for (int k = 0; k < kRopeVecPerThread; ++k) {
-    const int64_t v = v0 + threadIdx.x + k * kRopeThreads;
-    if (v < v1) {
-      a[k] = s0[v];
-      b[k] = s1[v];
-    }
-  }
   uint4* d0 = reinterpret_cast<uint4*>(p.dst0);
   uint4* d1 = reinterpret_cast<uint4*>(p.dst1);
 #pragma unroll

@@ -415,7 +415,10 @@ static sr_status rope_common(sr_session* s, const void* a_src, const void* b_src
   p.chunk_frames = s->cfg.chunk_frames;
   p.t_clock0 = s->cfg.t_clock0;
   p.mode = mode;
-  std::memcpy(p.inv_freq, s->inv_freq, sizeof(p.inv_freq));
+  for (int i = 0; i < 64; ++i) {
+    p.inv_freq_hi[i] = static_cast<float>(s->inv_freq[i]);
+    p.inv_freq_lo[i] = static_cast<float>(s->inv_freq[i] - static_cast<double>(p.inv_freq_hi[i]));
+  }
   std::memcpy(p.axis, s->axis, sizeof(p.axis));
   cudaError_t e = sr::launch_rope(p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SR_OK : SR_ERR_CUDA;

@@ -57,7 +57,8 @@ cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim,
 
 // ------------------------------------------------------------ RoPE / commit
 struct RopeParams {
-  double inv_freq[64];         // per rotary pair: base^(-2i/d_axis)
+  float inv_freq_hi[64];       // per rotary pair: base^(-2i/d_axis) = hi + lo (two floats)
+  float inv_freq_lo[64];
   const __nv_bfloat16* src0;   // rotated
   const __nv_bfloat16* src1;   // rotated (mode 0) or copied (mode 1)
   __nv_bfloat16* dst0;

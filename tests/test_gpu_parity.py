@@ -21,7 +21,7 @@ def _built():
 
 # ------------------------------------------------------------------ RoPE / commit
 
-@pytest.mark.parametrize("config,fill,clock", [(1, 0, 0), (1, 3, 7), (2, 6, 0), (2, 2, 1000)])
+@pytest.mark.parametrize("config,fill,clock", [(1, 0, 0), (1, 3, 7), (1, 2, 123457), (2, 6, 0), (2, 2, 1000)])
 def test_rope3d_qk_matches_oracle(config, fill, clock):
     shape = syn.SHAPES[config]
     tw = Twin(shape, config, fill=fill, t_clock0=clock)
