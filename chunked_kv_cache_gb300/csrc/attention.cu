@@ -21,7 +21,8 @@
 // Warp roles:
 //   warps 0-3   softmax group 0 (thread i owns row i of its tile)
 //   warps 4-7   softmax group 1
-//   warp 8      MMA issuer (one thread): tcgen05.mma, accumulators in TMEM
+//   warp 8      MMA issuer (the whole warp in step, one elected lane issues):
+//               tcgen05.mma, accumulators in TMEM
 //   warp 9      TMA producer (one thread): Q once, then K/V tiles through an
 //               NSTAGE-deep shared-memory ring, in the order the MMA consumes
 //   warps 10-11 idle (they complete the third warpgroup)
@@ -253,17 +254,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         for (int k = max(0, idx - nst); k < idx; ++k)
           wait_drain(&bars->kv_full[k % nst], (k / nst) & 1, p.timeout_ns);
       }
-    } else if (warp == kMmaWarp && lane == 0) {
+    } else if (warp == kMmaWarp) {
       // ---------------------------------------------------------- MMA issuer
+      // The whole warp runs this loop in step; one elected lane issues the
+      // MMAs and commits. Keeping the warp converged lets the descriptor and
+      // loop arithmetic run warp-uniform instead of as one divergent thread.
+      const uint32_t leader = elect_one();
       bool issued_any = false;
-      bool ok = wait_bounded(&bars->q_full, 0, wc, 2);
+      bool ok = __all_sync(0xffffffffu, wait_bounded(&bars->q_full, 0, wc, 2));
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
       int c = 0;   // consume counter, same order as the producer's loads
       const int nst = wk.split ? C::kStagesSplit : C::kStages;
       auto take = [&](int& stage) {
         stage = c % nst;
-        if (ok && !wait_bounded(&bars->kv_full[stage], (c / nst) & 1, wc, 3)) ok = false;
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->kv_full[stage], (c / nst) & 1, wc, 3));
         ++c;
       };
       // shared-memory address of a K/V stage (the extra split-mode stage is the second Q slot)
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           const uint32_t off = (kk / 4) * C::kAtomBytes + (kk % 4) * 32;
           const uint64_t ad = sdesc_sw128(qt + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(stage_addr(stage) + off, 16, 1024);
-          mma_ss(d_tmem, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
+          mma_ss_w(d_tmem, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u, leader);
         }
       };
       auto pv = [&](int t, int stage, bool acc) {   // O_t += P_t V
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(stage_addr(stage) + kk * 16 * 128, C::kAtomBytes, 1024);
-          mma_ts(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_w(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u, leader);
         }
       };
       const int n_it = wk.iters();
@@ -309,30 +314,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         for (int t = 0; t < 2; ++t) {
           const int cnt = wk.count(t);
           if (i > 0 && i - 1 < cnt) {
-            if (!wait_bounded(&bars->p_full[t], (i - 1) & 1, wc, 4)) {
+            if (!__all_sync(0xffffffffu, wait_bounded(&bars->p_full[t], (i - 1) & 1, wc, 4))) {
               ok = false;
               break;
             }
             tc_fence_after();
             pv(t, vs[t], i - 1 > 0);
-            if (i - 1 == cnt - 1) tc_commit(&bars->o_done[t]);
-            if (wk.split) tc_commit(&bars->kv_empty[vs[t]]);
+            if (i - 1 == cnt - 1) tc_commit_w(&bars->o_done[t], leader);
+            if (wk.split) tc_commit_w(&bars->kv_empty[vs[t]], leader);
           }
           if (i < cnt) {
             qk(t, ks[t]);
-            tc_commit(&bars->s_full[t]);
-            if (wk.split) tc_commit(&bars->kv_empty[ks[t]]);
+            tc_commit_w(&bars->s_full[t], leader);
+            if (wk.split) tc_commit_w(&bars->kv_empty[ks[t]], leader);
             issued_any = true;
           }
         }
         if (ok && !wk.split) {
-          if (i > 0) tc_commit(&bars->kv_empty[vs[0]]);
-          if (i < n_it) tc_commit(&bars->kv_empty[ks[0]]);
+          if (i > 0) tc_commit_w(&bars->kv_empty[vs[0]], leader);
+          if (i < n_it) tc_commit_w(&bars->kv_empty[ks[0]], leader);
         }
       }
       if (!ok && issued_any) {
         // no tensor-core work may still be running when TMEM is released
-        tc_commit(&bars->drain);
+        tc_commit_w(&bars->drain, leader);
         wait_drain(&bars->drain, 0, p.timeout_ns);
       }
     }
