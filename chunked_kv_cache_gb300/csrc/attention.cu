@@ -233,21 +233,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           tma_load_2d(dst + a * C::kAtomBytes, map, &bars->kv_full[stage], head * D + a * 64, row0, pol_kv);
         ++idx;
       };
-      // per iteration: the K tiles of iteration i, then the V tiles of i - 1
-      auto loads_of = [&](bool is_v, int i) {
-        if (wk.split) {
-          for (int t = 0; t < 2; ++t)
-            if (i < wk.count(t)) load(is_v, wk.kv(t, i));
-        } else {
-          load(is_v, i);
-        }
-      };
       const int n_it = wk.iters();
-      for (int i = 0; i < n_it && ok; ++i) {
-        loads_of(false, i);
-        if (i > 0) loads_of(true, i - 1);
+      if (!wk.split) {
+        // shared mode, per iteration: K_i, then V_{i-1}
+        for (int i = 0; i < n_it && ok; ++i) {
+          load(false, i);
+          if (i > 0) load(true, i - 1);
+        }
+        load(true, n_it - 1);
+      } else {
+        // split mode, in the order the MMAs consume them: per iteration and
+        // tile t, V(t, i-1) then K(t, i); every load then reuses a stage that
+        // was freed at least an iteration before it is needed
+        for (int i = 0; i <= n_it && ok; ++i)
+          for (int t = 0; t < 2; ++t) {
+            if (i > 0 && i - 1 < wk.count(t)) load(true, wk.kv(t, i - 1));
+            if (i < wk.count(t)) load(false, wk.kv(t, i));
+          }
       }
-      loads_of(true, n_it - 1);
       if (!ok || bars->abort) {
         // let every copy this CTA started land before shared memory is released
         wait_drain(&bars->q_full, 0, p.timeout_ns);
@@ -264,25 +267,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       bool ok = __all_sync(0xffffffffu, wait_bounded(&bars->q_full, 0, wc, 2));
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
-      int c = 0;   // consume counter, same order as the producer's loads
+      // Position in the producer's load sequence: stage and phase parity of
+      // the next load, advanced by counters (no division on this warp).
       const int nst = wk.split ? C::kStagesSplit : C::kStages;
-      auto take = [&](int& stage) {
-        stage = c % nst;
-        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->kv_full[stage], (c / nst) & 1, wc, 3));
-        ++c;
+      int st = 0;
+      uint32_t ph = 0;
+      auto take = [&]() -> int {   // wait for the next load; its stage
+        const int s0 = st;
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->kv_full[s0], ph, wc, 3));
+        if (++st == nst) {
+          st = 0;
+          ph ^= 1u;
+        }
+        return s0;
+      };
+      auto wait_p = [&](int t, int it) {   // softmax group t has written P_t of iteration it
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->p_full[t], it & 1, wc, 4));
+        tc_fence_after();
       };
       // shared-memory address of a K/V stage (the extra split-mode stage is the second Q slot)
       auto stage_addr = [&](int stage) -> uint32_t {
         return stage < C::kStages ? skv + stage * C::kTileBytes : sq + C::kTileBytes;
-      };
-      auto takes = [&](int i, int (&st)[2]) {
-        if (wk.split) {
-          for (int t = 0; t < 2; ++t)
-            if (i < wk.count(t)) take(st[t]);
-        } else {
-          take(st[0]);
-          st[1] = st[0];
-        }
       };
       auto qk = [&](int t, int stage) {   // S_t = Q_t K^T
         const uint32_t d_tmem = tmem + t * BN;
@@ -304,35 +309,104 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           mma_ts_w(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u, leader);
         }
       };
-      const int n_it = wk.iters();
-      int ks[2] = {0, 0}, vs[2] = {0, 0};
-      for (int i = 0; ok && i <= n_it; ++i) {
-        if (i < n_it) takes(i, ks);
-        if (i > 0) takes(i - 1, vs);
-        if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          const int cnt = wk.count(t);
-          if (i > 0 && i - 1 < cnt) {
-            if (!__all_sync(0xffffffffu, wait_bounded(&bars->p_full[t], (i - 1) & 1, wc, 4))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            pv(t, vs[t], i - 1 > 0);
-            if (i - 1 == cnt - 1) tc_commit_w(&bars->o_done[t], leader);
-            if (wk.split) tc_commit_w(&bars->kv_empty[vs[t]], leader);
+      if (!wk.split) {
+        // Shared mode: both tiles walk all n key tiles, and the loop carries
+        // nothing between two MMA bursts but the waits it cannot avoid. The
+        // tensor pipe queues only a few MMAs, so every cycle of other work
+        // between bursts (a division, a loop back edge, a branch) is a cycle
+        // the pipe may stand idle: stages advance by counters and the first
+        // and last iterations are peeled off, so the body branches only to
+        // leave on an abort.
+        const int n = wk.n;
+        // iteration 0: S_0 of both tiles
+        const int k0 = take();
+        if (ok) {
+          tc_fence_after();
+          qk(0, k0);
+          tc_commit_w(&bars->s_full[0], leader);
+          qk(1, k0);
+          tc_commit_w(&bars->s_full[1], leader);
+          tc_commit_w(&bars->kv_empty[k0], leader);
+          issued_any = true;
+        }
+        // iterations 1 .. n-1: PV_{i-1} and S_i of both tiles. The two takes
+        // come first, while the warp would otherwise be waiting for softmax
+        // group 0; between S0_i and PV1_{i-1} there is only that group's wait.
+        for (int i = 1; i < n && ok; ++i) {
+          const int ki = take();
+          const int vi = take();
+          tc_fence_after();
+          wait_p(0, i - 1);
+          if (!ok) break;
+          pv(0, vi, i > 1);
+          qk(0, ki);
+          tc_commit_w(&bars->s_full[0], leader);
+          wait_p(1, i - 1);
+          if (!ok) break;
+          pv(1, vi, i > 1);
+          qk(1, ki);
+          tc_commit_w(&bars->s_full[1], leader);
+          tc_commit_w(&bars->kv_empty[vi], leader);
+          tc_commit_w(&bars->kv_empty[ki], leader);
+        }
+        // last: PV_{n-1} of both tiles
+        if (ok) {
+          const int vl = take();
+          tc_fence_after();
+          wait_p(0, n - 1);
+          if (ok) {
+            pv(0, vl, n > 1);
+            tc_commit_w(&bars->o_done[0], leader);
+            wait_p(1, n - 1);
           }
-          if (i < cnt) {
-            qk(t, ks[t]);
-            tc_commit_w(&bars->s_full[t], leader);
-            if (wk.split) tc_commit_w(&bars->kv_empty[ks[t]], leader);
-            issued_any = true;
+          if (ok) {
+            pv(1, vl, n > 1);
+            tc_commit_w(&bars->o_done[1], leader);
+            tc_commit_w(&bars->kv_empty[vl], leader);
           }
         }
-        if (ok && !wk.split) {
-          if (i > 0) tc_commit_w(&bars->kv_empty[vs[0]], leader);
-          if (i < n_it) tc_commit_w(&bars->kv_empty[ks[0]], leader);
+      } else {
+        // Split mode (a single-tile last block): tile 0 walks c0 key tiles,
+        // tile 1 the next c1 (c0 - c1 is 0 or 1). The producer loads, per
+        // iteration i and tile t, V(t, i-1) then K(t, i); tile 1's waits come
+        // after tile 0's MMAs are queued.
+        const int c0 = wk.count(0), c1 = wk.count(1);
+        for (int i = 0; i <= c0 && ok; ++i) {
+          const bool p0 = i > 0 && i - 1 < c0, q0 = i < c0;
+          const int v0 = p0 ? take() : 0;
+          const int k0 = q0 ? take() : 0;
+          if (!ok) break;
+          tc_fence_after();
+          if (p0) {
+            wait_p(0, i - 1);
+            if (!ok) break;
+            pv(0, v0, i > 1);
+            if (i == c0) tc_commit_w(&bars->o_done[0], leader);
+            tc_commit_w(&bars->kv_empty[v0], leader);
+          }
+          if (q0) {
+            qk(0, k0);
+            tc_commit_w(&bars->s_full[0], leader);
+            tc_commit_w(&bars->kv_empty[k0], leader);
+            issued_any = true;
+          }
+          const bool p1 = i > 0 && i - 1 < c1, q1 = i < c1;
+          const int v1 = p1 ? take() : 0;
+          const int k1 = q1 ? take() : 0;
+          if (!ok) break;
+          tc_fence_after();
+          if (p1) {
+            wait_p(1, i - 1);
+            if (!ok) break;
+            pv(1, v1, i > 1);
+            if (i == c1) tc_commit_w(&bars->o_done[1], leader);
+            tc_commit_w(&bars->kv_empty[v1], leader);
+          }
+          if (q1) {
+            qk(1, k1);
+            tc_commit_w(&bars->s_full[1], leader);
+            tc_commit_w(&bars->kv_empty[k1], leader);
+          }
         }
       }
       if (!ok && issued_any) {
