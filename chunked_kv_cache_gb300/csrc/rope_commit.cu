@@ -8,11 +8,15 @@
 // index in the stream; section 3.3 "Persistent KV layout": the cache is
 // modified where it lives, never rebuilt.
 //
-// Work split: every thread moves 16-byte vectors (8 bf16 = 4 rotary pairs) of
-// token-major [L][H][d] rows, so loads and stores are fully coalesced. The
-// cos/sin of a token's d/2 pairs do not depend on the head: a CTA first fills a
-// small shared-memory table for the tokens it covers, then every head reuses it.
-// HBM bound: the kernel reads 2 and writes 2 tensors of L*H*d bf16 once.
+// Work split: a CTA takes whole tokens (tokens_per_cta of them, up to 1024
+// 16-byte vectors of each tensor), and every thread moves 16-byte vectors (8
+// bf16 = 4 rotary pairs) of the token-major [L][H][d] rows, so loads and
+// stores are fully coalesced. The cos/sin of a token's d/2 pairs do not depend
+// on the head: the CTA fills a small shared-memory table for its tokens while
+// its loads are in flight, and every head reuses it. Threads walk their
+// vectors with running (token, vector) counters, so no vector pays an integer
+// division. HBM bound: the kernel reads 2 and writes 2 tensors of L*H*d bf16
+// once.
 #include <cuda_bf16.h>
 
 #include "sr_kernels.h"
@@ -22,8 +26,8 @@ namespace sr {
 namespace {
 
 constexpr int kRopeThreads = 256;
-constexpr int kRopeVecPerThread = 4;
-constexpr int kRopeVecPerCta = kRopeThreads * kRopeVecPerThread;
+constexpr int kRopeVecPerThread = 4;     // per tensor and pass
+constexpr int kRopeVecTarget = kRopeThreads * kRopeVecPerThread;
 
 __device__ __forceinline__ uint32_t rotate_pair(uint32_t packed, float c, float s) {
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&packed);
@@ -36,18 +40,17 @@ __device__ __forceinline__ uint32_t rotate_pair(uint32_t packed, float c, float 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) {
-  extern __shared__ float2 cs_table[];  // [tokens of this CTA][D/2] (cos, sin)
+__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, int tokens_per_cta) {
   constexpr int kPairs = D / 2;
   constexpr int kVecPerHead = D / 8;
-  const int vec_per_tok = p.n_heads * kVecPerHead;
-  const int64_t total = static_cast<int64_t>(p.n_tok) * vec_per_tok;
-  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kRopeVecPerCta;
-  if (v0 >= total) return;
-  const int64_t v1 = min(v0 + kRopeVecPerCta, total);
-  const int tok_lo = static_cast<int>(v0 / vec_per_tok);
-  const int tok_hi = static_cast<int>((v1 - 1) / vec_per_tok);
-  const int ntok = tok_hi - tok_lo + 1;
+  extern __shared__ float2 smem_rope[];
+  float2* cs_table = smem_rope;                                               // [tokens_per_cta][D/2]
+  int32_t* dst_row = reinterpret_cast<int32_t*>(smem_rope + tokens_per_cta * kPairs);   // [tokens_per_cta]
+  const int vpt = p.n_heads * kVecPerHead;   // vectors per token
+  const int tok_lo = blockIdx.x * tokens_per_cta;
+  if (tok_lo >= p.n_tok) return;
+  const int ntok = min(tokens_per_cta, p.n_tok - tok_lo);
+  const int nvec = ntok * vpt;
 
   // Slot table: frame g = n + f now lives in slot g mod W.
   if (p.mode == 1 && blockIdx.x == 0 && threadIdx.x < p.chunk_frames) {
@@ -55,103 +58,123 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) 
     p.slot_frame[g % p.window_frames] = static_cast<int32_t>(g);
   }
 
-  // Loads first: they are in flight while the sin/cos table is built.
-  uint4 a[kRopeVecPerThread], b[kRopeVecPerThread];
-  const uint4* s0 = reinterpret_cast<const uint4*>(p.src0);
-  const uint4* s1 = reinterpret_cast<const uint4*>(p.src1);
-#pragma unroll
-  for (int k = 0; k < kRopeVecPerThread; ++k) {
-    const int64_t v = v0 + threadIdx.x + k * kRopeThreads;
-    if (v < v1) {
-      a[k] = s0[v];
-      b[k] = s1[v];
-    }
-  }
-
-  // Angle = pos * inv_freq, carried as an unevaluated sum of two floats (the
-  // rounded product, its exact FMA error, and pos times the low half of
-  // inv_freq), then reduced by 2*pi written as two floats (Cody-Waite) before
-  // the fp32 sincos. A plain fp32 product would carry an absolute error
-  // proportional to the angle (1e-4 rad at t ~ 1000); this keeps it ~1e-7.
-  for (int i = threadIdx.x; i < ntok * kPairs; i += kRopeThreads) {
-    const int tok = tok_lo + i / kPairs;
-    const int pr = i % kPairs;
-    const int ax = p.axis[pr];
-    const int in_frame = tok % p.tokens_per_frame;
-    int64_t pos;
-    if (ax == 0)
-      pos = p.t_clock0 + p.n_committed + tok / p.tokens_per_frame;
-    else if (ax == 1)
-      pos = in_frame / p.grid_w;
-    else
-      pos = in_frame % p.grid_w;
-    const float fp = static_cast<float>(pos);            // exact below 2^24
-    const float hi = p.inv_freq_hi[pr];
-    const float prod = fp * hi;
-    const float err = fmaf(fp, p.inv_freq_lo[pr], fmaf(fp, hi, -prod));
-    const float k = rintf(prod * 0.159154943091895336f);
-    float r = fmaf(-k, 6.28318548202514648f, prod);       // 2*pi rounded to float
-    r = fmaf(-k, -1.74845553146951906e-7f, r);            // 2*pi minus that float
-    r += err;
-    float sn, cs;
-    sincosf(r, &sn, &cs);
-    cs_table[i] = make_float2(cs, sn);
-  }
-  __syncthreads();
-
+  const uint4* s0 = reinterpret_cast<const uint4*>(p.src0) + static_cast<int64_t>(tok_lo) * vpt;
+  const uint4* s1 = reinterpret_cast<const uint4*>(p.src1) + static_cast<int64_t>(tok_lo) * vpt;
   uint4* d0 = reinterpret_cast<uint4*>(p.dst0);
   uint4* d1 = reinterpret_cast<uint4*>(p.dst1);
+
+  for (int base = 0; base < nvec; base += kRopeVecTarget) {
+    // Loads first: they are in flight while the sin/cos table is built.
+    uint4 a[kRopeVecPerThread], b[kRopeVecPerThread];
 #pragma unroll
-  for (int k = 0; k < kRopeVecPerThread; ++k) {
-    const int64_t v = v0 + threadIdx.x + k * kRopeThreads;
-    if (v >= v1) continue;
-    const int tok = static_cast<int>(v / vec_per_tok);
-    const int c8 = static_cast<int>(v % kVecPerHead);          // which 8-element group of the head
-    const float2* cs = cs_table + (tok - tok_lo) * kPairs + c8 * 4;
-    uint32_t* wa = reinterpret_cast<uint32_t*>(&a[k]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) wa[j] = rotate_pair(wa[j], cs[j].x, cs[j].y);
-    int64_t dst = v;
-    if (p.mode == 0) {
-      uint32_t* wb = reinterpret_cast<uint32_t*>(&b[k]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wb[j] = rotate_pair(wb[j], cs[j].x, cs[j].y);
-    } else {
-      // token -> ring row: frame f of the chunk goes to slot (n + f) mod W
-      const int f = tok / p.tokens_per_frame;
-      const int r = tok % p.tokens_per_frame;
-      const int slot = static_cast<int>((p.n_committed + f) % p.window_frames);
-      const int64_t row = static_cast<int64_t>(slot) * p.tokens_per_frame + r;
-      dst = row * vec_per_tok + (v % vec_per_tok);
+    for (int k = 0; k < kRopeVecPerThread; ++k) {
+      const int j = base + threadIdx.x + k * kRopeThreads;
+      if (j < nvec) {
+        a[k] = s0[j];
+        b[k] = s1[j];
+      }
     }
-    d0[dst] = a[k];
-    d1[dst] = b[k];
+
+    if (base == 0) {
+      // Angle = pos * inv_freq, carried as an unevaluated sum of two floats
+      // (the rounded product, its exact FMA error, and pos times the low half
+      // of inv_freq), then reduced by 2*pi written as two floats (Cody-Waite)
+      // before the fp32 sincos. A plain fp32 product would carry an absolute
+      // error proportional to the angle (1e-4 rad at t ~ 1000); this keeps it
+      // ~1e-7.
+      for (int i = threadIdx.x; i < ntok * kPairs; i += kRopeThreads) {
+        const int tok = tok_lo + i / kPairs;
+        const int pr = i % kPairs;
+        const int ax = p.axis[pr];
+        const int in_frame = tok % p.tokens_per_frame;
+        int64_t pos;
+        if (ax == 0)
+          pos = p.t_clock0 + p.n_committed + tok / p.tokens_per_frame;
+        else if (ax == 1)
+          pos = in_frame / p.grid_w;
+        else
+          pos = in_frame % p.grid_w;
+        const float fp = static_cast<float>(pos);            // exact below 2^24
+        const float hi = p.inv_freq_hi[pr];
+        const float prod = fp * hi;
+        const float err = fmaf(fp, p.inv_freq_lo[pr], fmaf(fp, hi, -prod));
+        const float k = rintf(prod * 0.159154943091895336f);
+        float r = fmaf(-k, 6.28318548202514648f, prod);       // 2*pi rounded to float
+        r = fmaf(-k, -1.74845553146951906e-7f, r);            // 2*pi minus that float
+        r += err;
+        float sn, cs;
+        sincosf(r, &sn, &cs);
+        cs_table[i] = make_float2(cs, sn);
+      }
+      // destination row of each token: itself (mode 0) or its ring row (mode 1),
+      // where frame f of the chunk goes to slot (n + f) mod W
+      for (int t = threadIdx.x; t < ntok; t += kRopeThreads) {
+        const int tok = tok_lo + t;
+        if (p.mode == 0) {
+          dst_row[t] = tok;
+        } else {
+          const int f = tok / p.tokens_per_frame;
+          const int r = tok - f * p.tokens_per_frame;
+          const int slot = static_cast<int>((p.n_committed + f) % p.window_frames);
+          dst_row[t] = slot * p.tokens_per_frame + r;
+        }
+      }
+      __syncthreads();
+    }
+
+    // this thread's first vector: token t, vector r within the token
+    int j = base + threadIdx.x;
+    int t = j / vpt;
+    int r = j - t * vpt;
+#pragma unroll
+    for (int k = 0; k < kRopeVecPerThread; ++k) {
+      if (j < nvec) {
+        const float2* cs = cs_table + t * kPairs + (r & (kVecPerHead - 1)) * 4;
+        uint32_t* wa = reinterpret_cast<uint32_t*>(&a[k]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wa[q] = rotate_pair(wa[q], cs[q].x, cs[q].y);
+        if (p.mode == 0) {
+          uint32_t* wb = reinterpret_cast<uint32_t*>(&b[k]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) wb[q] = rotate_pair(wb[q], cs[q].x, cs[q].y);
+        }
+        const int64_t dst = static_cast<int64_t>(dst_row[t]) * vpt + r;
+        d0[dst] = a[k];
+        d1[dst] = b[k];
+      }
+      j += kRopeThreads;
+      r += kRopeThreads;
+      while (r >= vpt) {
+        r -= vpt;
+        ++t;
+      }
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st) {
-  const int vec_per_tok = p.n_heads * head_dim / 8;
-  const int64_t total = static_cast<int64_t>(p.n_tok) * vec_per_tok;
-  if (total == 0) return cudaSuccess;
-  const int64_t grid = (total + kRopeVecPerCta - 1) / kRopeVecPerCta;
-  const int max_tok = kRopeVecPerCta / vec_per_tok + 2;
-  const size_t smem = static_cast<size_t>(max_tok) * (head_dim / 2) * sizeof(float2);
+  if (p.n_tok <= 0) return cudaSuccess;
+  const int vpt = p.n_heads * head_dim / 8;
+  const int tokens_per_cta = std::max(1, kRopeVecTarget / vpt);
+  const int grid = (p.n_tok + tokens_per_cta - 1) / tokens_per_cta;
+  const size_t smem = static_cast<size_t>(tokens_per_cta) * (head_dim / 2) * sizeof(float2) +
+                      static_cast<size_t>(tokens_per_cta) * sizeof(int32_t);
   if (head_dim == 128) {
     if (smem > 48 * 1024) {
       cudaError_t e = cudaFuncSetAttribute(rope_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    rope_kernel<128><<<static_cast<unsigned>(grid), kRopeThreads, smem, st>>>(p);
+    rope_kernel<128><<<static_cast<unsigned>(grid), kRopeThreads, smem, st>>>(p, tokens_per_cta);
   } else {
     if (smem > 48 * 1024) {
       cudaError_t e = cudaFuncSetAttribute(rope_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    rope_kernel<64><<<static_cast<unsigned>(grid), kRopeThreads, smem, st>>>(p);
+    rope_kernel<64><<<static_cast<unsigned>(grid), kRopeThreads, smem, st>>>(p, tokens_per_cta);
   }
   return cudaGetLastError();
 }
