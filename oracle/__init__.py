@@ -23,7 +23,11 @@ What it computes, and where the pages define it. The pages are
   evicted ([H3-page] 3.2 Iteration 3 item 2; 3.3 "Persistent KV layout").
 * ``session``    one static sink bank per denoising step ([H3-page] 3.3
   "Static-context KV caching"; [teardown] "A window that slides, and a prefix
-  that doesn't"), two steps then commit.
+  that doesn't"), two steps then commit; chunks of any number of frames and
+  a recent history of the last h committed frames.
+* ``schedule``   the scheduling units (2, 1, 1, 1 latents), the 7-unit first
+  window and the per-chunk plan ([teardown] "A window that slides, and a
+  prefix that doesn't"; [H3-page] 3.1.2).
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against closed
 forms, invariants, library routines or brute force; no function is
@@ -34,9 +38,11 @@ from .rope import axis_split, inverse_frequencies, token_positions, rope3d
 from .attention import attention, attention_rows
 from .ring import RingCache
 from .session import OracleSession
+from .schedule import chunk_plan, latent_rgb_frames, unit_latents, units_latents
 
 __all__ = [
     "bf16_bits_to_f64", "f64_to_bf16_bits", "round_bf16",
     "axis_split", "inverse_frequencies", "token_positions", "rope3d",
     "attention", "attention_rows", "RingCache", "OracleSession",
+    "chunk_plan", "latent_rgb_frames", "unit_latents", "units_latents",
 ]

@@ -33,7 +33,9 @@ class RingCache:
         self.slot_frame[s] = g
 
     def commit(self, k: np.ndarray, v: np.ndarray, frames: int):
-        """Append ``frames`` consecutive frames (k, v: [frames*T][H][d])."""
+        """Append ``frames`` consecutive frames (k, v: [frames*T][H][d]) in
+        stream order. When ``frames`` exceeds W the chunk's own later frames
+        evict its earlier ones, and only its last W frames stay."""
         for f in range(frames):
             g = self.n + f
             self.write_frame(g, k[f * self.T:(f + 1) * self.T], v[f * self.T:(f + 1) * self.T])
@@ -48,3 +50,18 @@ class RingCache:
             return np.empty(shape), np.empty(shape), occupied
         idx = np.concatenate([np.arange(s * self.T, (s + 1) * self.T) for s in occupied])
         return self.k[idx], self.v[idx], occupied
+
+    def recent(self, h: int):
+        """K and V of the last h committed frames (frames n-h .. n-1), in
+        stream order: the recent history of the next chunk."""
+        if h < 0 or h > min(self.n, self.W):
+            raise ValueError("history longer than what the ring holds")
+        frames = list(range(self.n - h, self.n))
+        for g in frames:
+            if self.slot_frame[self.slot_of(g)] != g:
+                raise ValueError(f"frame {g} is no longer in the ring")
+        if not frames:
+            shape = (0,) + self.k.shape[1:]
+            return np.empty(shape), np.empty(shape), frames
+        idx = np.concatenate([np.arange(self.slot_of(g) * self.T, (self.slot_of(g) + 1) * self.T) for g in frames])
+        return self.k[idx], self.v[idx], frames

@@ -58,29 +58,35 @@ class OracleSession:
         self.ring.slot_frame[:] = slot_frame
         self.ring.n = n_committed
 
-    def chunk_positions(self):
-        return token_positions(self.F * self.T, self.grid_h, self.grid_w,
+    def chunk_positions(self, frames=None):
+        frames = self.F if frames is None else frames
+        return token_positions(frames * self.T, self.grid_h, self.grid_w,
                                self.t_clock0 + self.ring.n)
 
-    def rope3d_qk(self, q_bits, k_bits):
-        """Rotate the chunk's Q and K at frames n .. n+F-1; bf16 bits out."""
-        t, h, w = self.chunk_positions()
+    def rope3d_qk(self, q_bits, k_bits, frames=None):
+        """Rotate the chunk's Q and K at frames n .. n+F-1 (F = ``frames``,
+        default the configured chunk length); bf16 bits out."""
+        t, h, w = self.chunk_positions(frames)
         q = rope3d(bf16_bits_to_f64(q_bits), t, h, w, self.base)
         k = rope3d(bf16_bits_to_f64(k_bits), t, h, w, self.base)
         return f64_to_bf16_bits(q), f64_to_bf16_bits(k)
 
-    def visible_kv(self, step, k_bits, v_bits):
-        rk, rv, _ = self.ring.visible()
+    def visible_kv(self, step, k_bits, v_bits, hist=None):
+        """bank[step], then the ring's frames (every occupied slot, or only
+        the last ``hist`` committed frames), then the chunk."""
+        rk, rv, _ = self.ring.visible() if hist is None else self.ring.recent(hist)
         k = np.concatenate([self.sink_k[step], rk, bf16_bits_to_f64(k_bits)], axis=0)
         v = np.concatenate([self.sink_v[step], rv, bf16_bits_to_f64(v_bits)], axis=0)
         return k, v
 
-    def chunk_attention(self, step, q_bits, k_bits, v_bits, rows=None, heads=None):
+    def chunk_attention(self, step, q_bits, k_bits, v_bits, rows=None, heads=None, hist=None):
         """Attention of the (already rotated) chunk queries for denoising
-        step ``step``. Optionally only for a sample of rows and heads."""
+        step ``step``, over the ring's occupied frames or, with ``hist``, its
+        last ``hist`` committed frames. Optionally only for a sample of rows
+        and heads."""
         if not 0 <= step < self.n_steps:
             raise ValueError("step out of range")
-        k, v = self.visible_kv(step, k_bits, v_bits)
+        k, v = self.visible_kv(step, k_bits, v_bits, hist)
         q = bf16_bits_to_f64(q_bits)
         if rows is not None:
             q = q[np.asarray(rows)]
@@ -89,17 +95,19 @@ class OracleSession:
             q, k, v = q[:, heads], k[:, heads], v[:, heads]
         return attention(q, k, v, self.scale)
 
-    def cache_commit(self, k_raw_bits, v_bits):
+    def cache_commit(self, k_raw_bits, v_bits, frames=None):
         """Rotate the clean chunk's K at its frame positions, round K and V
-        to bf16 and write frames n .. n+F-1 into slots (n+f) mod W."""
-        t, h, w = self.chunk_positions()
+        to bf16 and write frames n .. n+F-1 into slots (n+f) mod W (F =
+        ``frames``, default the configured chunk length)."""
+        frames = self.F if frames is None else frames
+        t, h, w = self.chunk_positions(frames)
         k = rope3d(bf16_bits_to_f64(k_raw_bits), t, h, w, self.base)
         k = bf16_bits_to_f64(f64_to_bf16_bits(k))
         v = bf16_bits_to_f64(v_bits)
         if self.W == 0:
-            self.ring.n += self.F
+            self.ring.n += frames
             return
-        self.ring.commit(k, v, self.F)
+        self.ring.commit(k, v, frames)
 
     def ring_bits(self):
         return f64_to_bf16_bits(self.ring.k), f64_to_bf16_bits(self.ring.v)

@@ -7,6 +7,11 @@ Session: the visible-set size of the H3 project page's worked example
 evicted and future chunks change nothing), and clock-shift invariance of
 the scores (the Iteration 4 fix: a score is a function of the gap in time,
 not of absolute time).
+Chunks of varying length and a recent-history window (the unit rhythm):
+recent(h) against a plain list of every committed frame (including commits
+longer than the ring), positions of a chunk of any length from the frame
+counter, and attention with a history window against the same visible set
+assembled by hand.
 """
 import collections
 import math
@@ -16,7 +21,7 @@ import numpy as np
 import pytest
 
 import synthetic as syn
-from oracle import (OracleSession, RingCache, attention, bf16_bits_to_f64, rope3d,
+from oracle import (OracleSession, RingCache, attention, bf16_bits_to_f64, f64_to_bf16_bits, rope3d,
                     token_positions)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -154,3 +159,82 @@ def test_commit_rotates_keys_at_absolute_frames():
     got = a.ring.k[3 * T:4 * T]
     assert np.allclose(got, want, rtol=2.0 ** -8, atol=1e-30)
     assert np.array_equal(a.ring.v[3 * T:4 * T], bf16_bits_to_f64(x1.clean_v)[T:2 * T])
+
+
+# ---- chunks of varying length and a recent-history window (the unit rhythm)
+
+def test_recent_history_against_a_list_of_committed_frames():
+    # commits of 9, 3, 2, 3, 2, ... frames (the page's first window, then the
+    # alternating chunks) into a ring of W frames; recent(h) must return the
+    # last h frames in stream order, taken from a plain list of every frame
+    T, H, d = 2, 1, 1
+    for W in (3, 4, 5):
+        ring = RingCache(W, T, H, d)
+        stream = []
+        for F in [9, 3, 2, 3, 2, 3, 2, 3]:
+            frames = np.arange(ring.n, ring.n + F, dtype=np.float64)
+            k = np.repeat(frames, T)[:, None, None]
+            ring.commit(k, -k, F)
+            stream.extend(range(ring.n - F, ring.n))
+            kept = stream[-W:]
+            assert sorted(g for g in ring.slot_frame if g >= 0) == kept   # later frames of one commit evict earlier ones
+            for h in range(0, min(ring.n, W) + 1):
+                rk, rv, fr = ring.recent(h)
+                assert fr == stream[len(stream) - h:]
+                assert np.array_equal(rk[:, 0, 0], np.repeat(np.array(fr, np.float64), T))
+                assert np.array_equal(rv, -rk)
+            with pytest.raises(ValueError):
+                ring.recent(min(ring.n, W) + 1)
+
+
+def test_chunk_of_other_length_takes_positions_from_the_frame_counter():
+    shape = syn.TINY
+    a = _session(shape, t_clock0=7)
+    T = shape.tokens_per_frame
+    g = np.random.default_rng(3)
+    for F in (3, 1, 2):
+        n0 = a.n_committed
+        x = g.standard_normal((F * T, shape.n_heads, shape.head_dim))
+        bits = f64_to_bf16_bits(x)
+        q, _ = a.rope3d_qk(bits, bits, frames=F)
+        t, h, w = token_positions(F * T, shape.grid_h, shape.grid_w, 7 + n0)
+        assert t[0] == 7 + n0 and t[-1] == 7 + n0 + F - 1
+        assert np.array_equal(q, f64_to_bf16_bits(rope3d(bf16_bits_to_f64(bits), t, h, w, 1e4)))
+        a.cache_commit(bits, bits, frames=F)
+        assert a.n_committed == n0 + F
+
+
+def test_history_window_selects_exactly_the_last_frames():
+    # with hist = h the visible set is bank[step] + frames n-h .. n-1 + chunk,
+    # and the output equals attention over that set assembled by hand
+    shape = syn.TINY
+    a = _session(shape)
+    T = shape.tokens_per_frame
+    g = np.random.default_rng(5)
+    kept = {}
+    for F in (3, 2, 3):
+        k = f64_to_bf16_bits(g.standard_normal((F * T, shape.n_heads, shape.head_dim)))
+        v = f64_to_bf16_bits(g.standard_normal((F * T, shape.n_heads, shape.head_dim)))
+        n0 = a.n_committed
+        a.cache_commit(k, v, frames=F)
+        for f in range(F):
+            kept[n0 + f] = (a.ring.k[((n0 + f) % a.W) * T:((n0 + f) % a.W + 1) * T].copy(),
+                            bf16_bits_to_f64(v)[f * T:(f + 1) * T])
+    n = a.n_committed                     # 8 frames committed into W = 4 slots
+    F = 2
+    q = f64_to_bf16_bits(g.standard_normal((F * T, shape.n_heads, shape.head_dim)))
+    ck = f64_to_bf16_bits(g.standard_normal((F * T, shape.n_heads, shape.head_dim)))
+    cv = f64_to_bf16_bits(g.standard_normal((F * T, shape.n_heads, shape.head_dim)))
+    for h in (0, 2, 3, 4):
+        kk, _ = a.visible_kv(0, ck, cv, hist=h)
+        assert kk.shape[0] == shape.n_sink + h * T + F * T
+        hk = np.concatenate([kept[gg][0] for gg in range(n - h, n)] or [np.empty((0, shape.n_heads, shape.head_dim))])
+        hv = np.concatenate([kept[gg][1] for gg in range(n - h, n)] or [np.empty((0, shape.n_heads, shape.head_dim))])
+        K = np.concatenate([a.sink_k[0], hk, bf16_bits_to_f64(ck)])
+        V = np.concatenate([a.sink_v[0], hv, bf16_bits_to_f64(cv)])
+        want, _ = attention(bf16_bits_to_f64(q), K, V, a.scale)
+        got, _ = a.chunk_attention(0, q, ck, cv, hist=h)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    full, _ = a.chunk_attention(0, q, ck, cv)
+    last_w, _ = a.chunk_attention(0, q, ck, cv, hist=a.W)
+    assert np.allclose(full, last_w, rtol=1e-12, atol=1e-12)   # the whole ring = the last W frames
