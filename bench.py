@@ -9,6 +9,10 @@ used alternately, so every step reads inputs that were last touched more
 than an L2's worth of traffic ago.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2|3]
+                    [--workload steady|rhythm]
+
+``--workload rhythm`` times the pages' unit rhythm instead (chunks of 3 and 2
+latent frames at the 832x480 frame size) and prints its own line.
 
 Multi-GPU: the path has no exchange step, so N ranks run N independent
 replicas (weak scaling, no collective on the data path); rank 0 prints the
@@ -400,6 +404,111 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_rhythm(args):
+    """The pages' unit rhythm at the 832x480 frame size: after the 9-latent
+    first window, chunks alternate 3 latents (2 latents of history) and 2
+    latents (3 of history); the ring holds W = 3 latent frames. One bench step
+    = one chunk (2 x (RoPE + attention) + commit), steps alternating the two
+    chunk kinds; two sessions are used alternately, as in the main workload."""
+    import chunked_kv_cache_gb300 as sr
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_kv_cache_gb300 import build
+    build.build()
+    base = syn.SHAPES[2]
+    W, Fmax = 3, 9
+    T, H, d, S = base.tokens_per_frame, base.n_heads, base.head_dim, base.n_sink
+    sessions = []
+    for sid in range(2):
+        sink = lambda tid: syn.device_normal_bf16((base.n_steps, S, H, d), dev, 5, sid, 0, 0, tid)
+        s = sr.Session(H, d, base.grid_h, base.grid_w, 3, W, S, base.n_steps, sink_k=sink(syn.T_SINK_K),
+                       sink_v=sink(syn.T_SINK_V), device=dev)
+        xs = {}
+        for F in (2, 3, Fmax):
+            dims = (F * T, H, d)
+            xs[F] = {k: [syn.device_normal_bf16(dims, dev, 5, sid, F, st, tid) for st in range(base.n_steps)]
+                     for k, tid in (("q", syn.T_Q), ("k", syn.T_K), ("v", syn.T_V))}
+            xs[F]["clean_k"] = syn.device_normal_bf16(dims, dev, 5, sid, F, 0, syn.T_CLEAN_K)
+            xs[F]["clean_v"] = syn.device_normal_bf16(dims, dev, 5, sid, F, 0, syn.T_CLEAN_V)
+            xs[F]["o"] = torch.empty(dims, dtype=torch.bfloat16, device=dev)
+        sessions.append([s, xs, 0])          # session, inputs, next chunk index
+
+    def chunk(entry, ev=None):
+        s, xs, c = entry
+        plan = sr.plan_chunk(c)
+        F, h = plan["n_frames"], min(plan["hist_frames"], W)
+        x = xs[F]
+        for st in range(base.n_steps):
+            s.rope3d_qk(x["q"][st], x["k"][st], frames=F)
+            if ev is not None:
+                ev[st][0].record()
+            s.chunk_attention(st, x["q"][st], x["k"][st], x["v"][st], out=x["o"], frames=F, hist=h)
+            if ev is not None:
+                ev[st][1].record()
+        s.cache_commit(x["clean_k"], x["clean_v"], frames=F)
+        entry[2] = c + 1
+        return F, h
+
+    # first window, then warm-up chunks in pairs, so that every session's next
+    # chunk is a 3-latent one and the timed steps alternate 3 and 2 latents
+    for e in sessions:
+        for _ in range(1 + 2 * max(2, args.warmup // 2)):
+            chunk(e)
+    torch.cuda.synchronize()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    steps = max(2, args.steps - args.steps % 2)
+    evs = [[mk() for _ in range(base.n_steps)] for _ in range(steps)]
+    kinds = []
+    t0, t1 = mk()
+    with Clocks(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        t0.record()
+        for i in range(steps):
+            kinds.append(chunk(sessions[(i // 2) % 2], evs[i]))
+        t1.record()
+        torch.cuda.synchronize()
+    for s, _, _ in sessions:
+        if s.error_status() != 0:
+            raise RuntimeError("device error word set during the bench")
+    elapsed = t0.elapsed_time(t1) / 1e3
+    peak_tf, _, peak_kind = _peaks()
+    per_kind = {}
+    tot_fl, tot_ms = 0.0, 0.0
+    for (F, h), ev in zip(kinds, evs):
+        lq, lk = F * T, S + h * T + F * T
+        fl = 4.0 * H * lq * lk * d
+        ms = [a.elapsed_time(b) for a, b in ev]
+        k = f"{F}_latents"
+        e = per_kind.setdefault(k, {"lq": lq, "lk": lk, "hist_frames": h, "attn_ms": [], "flops": fl})
+        e["attn_ms"].extend(ms)
+        tot_fl += fl * len(ms)
+        tot_ms += sum(ms)
+    for e in per_kind.values():
+        m = statistics.mean(e.pop("attn_ms"))
+        e["attention_ms_per_denoise_step"] = round(m, 4)
+        e["attention_tflops"] = round(e.pop("flops") / (m / 1e3) / 1e12, 2)
+    achieved = tot_fl / (tot_ms / 1e3) / 1e12
+    out = {
+        "metric": "unit-rhythm chunk attention TFLOP/s and ms per chunk on 1 GB300", "value": round(achieved, 2),
+        "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_chunk": round(elapsed / steps * 1e3, 4), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "832x480 latent frames (24x128, 30x52 grid, S=2072), the pages' unit rhythm: "
+                               "9-latent first window, then chunks of 3 and 2 latents with 2 and 3 latents of "
+                               "recent history, ring W=3; one step = one chunk: 2 x (RoPE-3D + attention) + commit",
+                   "l2": "two sessions used alternately"},
+        "chunks": per_kind,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4), "kernel": "attn_kernel (sr_chunk_attention_frames)",
+                     "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "clocks": clk.summary(),
+        "gpu_launches": 5 * steps,
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,6 +516,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, choices=[2, 3], default=2)
+    ap.add_argument("--workload", choices=["steady", "rhythm"], default="steady",
+                    help="steady: the headline chunk workload; rhythm: the pages' 3/2-latent unit rhythm")
     ap.add_argument("--profile", action="store_true",
                     help="under a profiler: skip the end-to-end and CPU-baseline legs (their numbers are not reported)")
     args = ap.parse_args()
@@ -414,6 +525,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "rhythm":
+        run_rhythm(args)
     else:
         run_ours(args)
 

@@ -14,13 +14,15 @@ from . import _native
 from ._native import (SrConfig, SrBuffers, SrError, sr_session_init, sr_session_restore, sr_session_frames,
                       sr_rope3d_qk, sr_chunk_attention, sr_cache_commit, sr_session_free,
                       sr_chunk_attention_batch, sr_device_error_status, sr_debug_wait_timeout,
-                      sr_workspace_bytes, SR_MAX_BATCH)
+                      sr_workspace_bytes, sr_plan_chunk, sr_rope3d_qk_frames, sr_chunk_attention_frames,
+                      sr_cache_commit_frames, SrChunkPlan, SR_MAX_BATCH)
 
 __all__ = [
     "Session", "chunk_attention_batch", "SrConfig", "SrBuffers", "SrError",
     "sr_session_init", "sr_session_restore", "sr_session_frames", "sr_rope3d_qk", "sr_chunk_attention",
     "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch", "sr_device_error_status",
-    "sr_debug_wait_timeout", "sr_workspace_bytes",
+    "sr_debug_wait_timeout", "sr_workspace_bytes", "sr_plan_chunk", "sr_rope3d_qk_frames",
+    "sr_chunk_attention_frames", "sr_cache_commit_frames", "SrChunkPlan", "plan_chunk",
 ]
 
 _BF16 = torch.bfloat16
@@ -99,37 +101,54 @@ class Session:
         """Synchronises the stream and maps the device error word to a status."""
         return sr_device_error_status(int(self.err_word.item()))
 
-    def _chunk(self, name: str, t: torch.Tensor) -> None:
-        _check_tensor(name, t, (self.lq, self.H, self.d), self.device)
+    def _chunk(self, name: str, t: torch.Tensor, frames: int | None = None) -> None:
+        rows = self.lq if frames is None else frames * self.T
+        _check_tensor(name, t, (rows, self.H, self.d), self.device)
 
     # ---------------------------------------------------------------- calls
-    def rope3d_qk(self, q: torch.Tensor | None, k: torch.Tensor | None) -> None:
+    # frames=None: the configured chunk length and the plain C calls; an int:
+    # a chunk of that many frames through the *_frames calls (the unit rhythm).
+    def rope3d_qk(self, q: torch.Tensor | None, k: torch.Tensor | None, frames: int | None = None) -> None:
         for name, t in (("q", q), ("k", k)):
             if t is not None:
-                self._chunk(name, t)
-        sr_rope3d_qk(self.handle, _ptr(q), _ptr(k), _stream(self.device))
+                self._chunk(name, t, frames)
+        if frames is None:
+            sr_rope3d_qk(self.handle, _ptr(q), _ptr(k), _stream(self.device))
+        else:
+            sr_rope3d_qk_frames(self.handle, frames, _ptr(q), _ptr(k), _stream(self.device))
 
     def chunk_attention(self, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
-                        out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = None):
+                        out: torch.Tensor | None = None, lse: torch.Tensor | bool | None = None,
+                        frames: int | None = None, hist: int | None = None):
+        """hist: visible recent history in frames (None: every occupied slot)."""
         for name, t in (("q", q), ("k", k), ("v", v)):
-            self._chunk(name, t)
+            self._chunk(name, t, frames)
         if out is None:
             out = torch.empty_like(q)
-        self._chunk("out", out)
+        self._chunk("out", out, frames)
+        rows = q.shape[0]
         if lse is True:
-            lse = torch.empty((self.H, self.lq), dtype=torch.float32, device=self.device)
+            lse = torch.empty((self.H, rows), dtype=torch.float32, device=self.device)
         if isinstance(lse, torch.Tensor):
-            _check_tensor("lse", lse, (self.H, self.lq), self.device, torch.float32)
+            _check_tensor("lse", lse, (self.H, rows), self.device, torch.float32)
         else:
             lse = None
-        sr_chunk_attention(self.handle, step, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                           _ptr(lse), _stream(self.device))
+        if frames is None and hist is None:
+            sr_chunk_attention(self.handle, step, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               _ptr(lse), _stream(self.device))
+        else:
+            sr_chunk_attention_frames(self.handle, step, self.F if frames is None else frames,
+                                      -1 if hist is None else hist, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                      out.data_ptr(), _ptr(lse), _stream(self.device))
         return (out, lse) if lse is not None else out
 
-    def cache_commit(self, k: torch.Tensor, v: torch.Tensor) -> None:
-        self._chunk("k", k)
-        self._chunk("v", v)
-        sr_cache_commit(self.handle, k.data_ptr(), v.data_ptr(), _stream(self.device))
+    def cache_commit(self, k: torch.Tensor, v: torch.Tensor, frames: int | None = None) -> None:
+        self._chunk("k", k, frames)
+        self._chunk("v", v, frames)
+        if frames is None:
+            sr_cache_commit(self.handle, k.data_ptr(), v.data_ptr(), _stream(self.device))
+        else:
+            sr_cache_commit_frames(self.handle, frames, k.data_ptr(), v.data_ptr(), _stream(self.device))
 
     def close(self) -> None:
         if self.handle is not None:
@@ -141,6 +160,16 @@ class Session:
             self.close()
         except Exception:
             pass
+
+
+def plan_chunk(chunk_index: int, bootstrap_units: int = 7, chunk_units: int = 2, window_units: int = 2,
+               sink_units: int = 2, merge_single_frame_units: bool = True) -> dict:
+    """The unit rhythm's plan for one chunk (host arithmetic in libsr.so):
+    first_frame, n_frames, hist_frames, sink_frames."""
+    p = sr_plan_chunk(chunk_index, bootstrap_units, chunk_units, window_units, sink_units,
+                      merge_single_frame_units)
+    return {"first_frame": p.first_frame, "n_frames": p.n_frames, "hist_frames": p.hist_frames,
+            "sink_frames": p.sink_frames}
 
 
 def chunk_attention_batch(sessions, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -27,7 +27,8 @@ EXPORTS = (
     "sr_session_init", "sr_session_restore", "sr_session_frames", "sr_rope3d_qk",
     "sr_chunk_attention", "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch",
     "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string", "sr_workspace_bytes",
-    "sr_chunk_attention_noalloc",
+    "sr_chunk_attention_noalloc", "sr_plan_chunk", "sr_rope3d_qk_frames", "sr_chunk_attention_frames",
+    "sr_cache_commit_frames",
 )
 
 
@@ -49,6 +50,13 @@ class SrBuffers(ctypes.Structure):
         ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p),
         ("slot_frame", ctypes.c_void_p), ("err_word", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
+    ]
+
+
+class SrChunkPlan(ctypes.Structure):
+    _fields_ = [
+        ("first_frame", ctypes.c_int32), ("n_frames", ctypes.c_int32),
+        ("hist_frames", ctypes.c_int32), ("sink_frames", ctypes.c_int32),
     ]
 
 
@@ -79,6 +87,10 @@ def lib() -> ctypes.CDLL:
         L.sr_cache_commit.argtypes = [vp, vp, vp, vp]
         L.sr_chunk_attention_noalloc.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
         L.sr_session_free.argtypes = [vp]
+        L.sr_plan_chunk.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(SrChunkPlan)]
+        L.sr_rope3d_qk_frames.argtypes = [vp, i32, vp, vp, vp]
+        L.sr_chunk_attention_frames.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.sr_cache_commit_frames.argtypes = [vp, i32, vp, vp, vp]
         L.sr_chunk_attention_batch.argtypes = [ctypes.POINTER(vp), i32, i32, vp, vp, vp,
                                                ctypes.POINTER(i64), vp, vp, vp]
         L.sr_device_error_status.argtypes = [i32]
@@ -132,6 +144,30 @@ def sr_rope3d_qk(handle: int, q: int, k: int, stream: int) -> None:
 def sr_chunk_attention(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int, stream: int) -> None:
     _check(lib().sr_chunk_attention(handle, int(step), q, k, v, o, lse or None, stream or None),
            "sr_chunk_attention")
+
+
+def sr_plan_chunk(chunk_index: int, bootstrap_units: int = 7, chunk_units: int = 2, window_units: int = 2,
+                  sink_units: int = 2, merge_single_frame_units: bool = True) -> SrChunkPlan:
+    out = SrChunkPlan()
+    _check(lib().sr_plan_chunk(int(chunk_index), int(bootstrap_units), int(chunk_units), int(window_units),
+                               int(sink_units), 1 if merge_single_frame_units else 0, ctypes.byref(out)),
+           "sr_plan_chunk")
+    return out
+
+
+def sr_rope3d_qk_frames(handle: int, n_frames: int, q: int, k: int, stream: int) -> None:
+    _check(lib().sr_rope3d_qk_frames(handle, int(n_frames), q or None, k or None, stream or None),
+           "sr_rope3d_qk_frames")
+
+
+def sr_chunk_attention_frames(handle: int, step: int, n_frames: int, hist_frames: int, q: int, k: int, v: int,
+                              o: int, lse: int, stream: int) -> None:
+    _check(lib().sr_chunk_attention_frames(handle, int(step), int(n_frames), int(hist_frames), q, k, v, o,
+                                           lse or None, stream or None), "sr_chunk_attention_frames")
+
+
+def sr_cache_commit_frames(handle: int, n_frames: int, k_raw: int, v: int, stream: int) -> None:
+    _check(lib().sr_cache_commit_frames(handle, int(n_frames), k_raw, v, stream or None), "sr_cache_commit_frames")
 
 
 def sr_chunk_attention_noalloc(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int,

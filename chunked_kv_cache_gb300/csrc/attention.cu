@@ -1,7 +1,7 @@
 // attention.cu -- streaming chunk attention on the sm_103a tensor cores.
 //
 // O = softmax(scale * Q K^T) V for the chunk's queries over
-//     sink bank[step]  U  occupied ring frames  U  the chunk's own keys,
+//     sink bank[step]  U  visible ring frames  U  the chunk's own keys,
 // with no mask: every chunk query sees every visible key, in both time
 // directions (H3 project page, "Interactive Coding Worlds with Real-time
 // Streaming Diffusion Render", section 3.1.2 and its "Prefix cache"
@@ -95,10 +95,10 @@ struct SmemBars {
 };
 
 struct TileMap {
-  int nt[3];
+  int nt[kSegs];
   __device__ __forceinline__ void locate(int j, int& seg, int& row0) const {
     seg = 0;
-    while (seg < 2 && j >= nt[seg]) {
+    while (seg < kSegs - 1 && j >= nt[seg]) {
       j -= nt[seg];
       ++seg;
     }
@@ -163,8 +163,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int n_qtiles = min(2, (S.lq - q_local0 + BM - 1) / BM);
   TileMap tm;
 #pragma unroll
-  for (int s = 0; s < 3; ++s) tm.nt[s] = (S.seg_rows[s] + BN - 1) / BN;
-  const int n_kv_all = tm.nt[0] + tm.nt[1] + tm.nt[2];
+  int n_kv_all = 0;
+#pragma unroll
+  for (int s = 0; s < kSegs; ++s) {
+    tm.nt[s] = (S.seg_rows[s] + BN - 1) / BN;
+    n_kv_all += tm.nt[s];
+  }
   // a single-tile last block may be one of `parts` CTAs sharing its key range
   const int parts = (n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
   const int kv_lo = static_cast<int>(static_cast<int64_t>(part) * n_kv_all / parts);
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       tma_prefetch_map(&p.qmap);
-      for (int s = 0; s < 3; ++s)
+      for (int s = 0; s < kSegs; ++s)
         if (tm.nt[s]) {
           tma_prefetch_map(&S.kmap[s]);
           tma_prefetch_map(&S.vmap[s]);

@@ -53,9 +53,11 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, 
   const int nvec = ntok * vpt;
 
   // Slot table: frame g = n + f now lives in slot g mod W.
-  if (p.mode == 1 && blockIdx.x == 0 && threadIdx.x < p.chunk_frames) {
-    const int64_t g = p.n_committed + threadIdx.x;
-    p.slot_frame[g % p.window_frames] = static_cast<int32_t>(g);
+  if (p.mode == 1 && blockIdx.x == 0) {
+    for (int f = threadIdx.x; f < p.chunk_frames; f += kRopeThreads) {
+      const int64_t g = p.n_committed + f;
+      p.slot_frame[g % p.window_frames] = static_cast<int32_t>(g);
+    }
   }
 
   const uint4* s0 = reinterpret_cast<const uint4*>(p.src0) + static_cast<int64_t>(tok_lo) * vpt;

@@ -139,37 +139,78 @@ cudaError_t ensure_attn_attr(int head_dim, int nsess_template) {
   return e;
 }
 
+// What one attention call of a session sees: the chunk's query/key rows and
+// how many of the most recent committed frames are visible.
+struct ChunkView {
+  int64_t lq;     // chunk rows, frames * T
+  int64_t hist;   // visible history: the last `hist` committed frames
+};
+
+// The plain calls: the configured chunk length and every occupied slot.
+ChunkView default_view(const sr_session* s) {
+  return {s->lq, std::min<int64_t>(s->n_committed, s->cfg.window_frames)};
+}
+
+// Ring rows holding frames n-hist .. n-1, as one or two contiguous ranges
+// [r0, r0 + c0) and [0, c1) (the second when they wrap around the end of the
+// ring). All W slots at once are one range whatever the order.
+void ring_ranges(const sr_session* s, int64_t hist, int64_t& r0, int64_t& c0, int64_t& c1) {
+  const int64_t W = s->cfg.window_frames, T = s->tokens_per_frame;
+  r0 = c0 = c1 = 0;
+  if (hist <= 0 || W == 0) return;
+  if (hist >= W) {
+    c0 = W * T;
+    return;
+  }
+  const int64_t start = (s->n_committed - hist) % W;
+  if (start + hist <= W) {
+    r0 = start * T;
+    c0 = hist * T;
+  } else {
+    r0 = start * T;
+    c0 = (W - start) * T;
+    c1 = (start + hist - W) * T;
+  }
+}
+
 // Fill one session's segment maps for `step` (rows of the chunk taken from
 // k, v at row offset `row0` of a packed tensor).
-sr_status fill_session(sr::AttnSession& out, sr_session* s, int step, const void* k, const void* v,
-                       int64_t row0) {
+sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& view, int step, const void* k,
+                       const void* v, int64_t row0) {
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
+  const size_t row_bytes = static_cast<size_t>(row_elems) * 2;
   const int64_t S = s->cfg.n_sink;
-  const int64_t W = s->cfg.window_frames;
-  const int64_t valid_frames = std::min<int64_t>(s->n_committed, W);
-  const int64_t ring_rows = valid_frames * s->tokens_per_frame;
+  int64_t r0 = 0, c0 = 0, c1 = 0;
+  ring_ranges(s, view.hist, r0, c0, c1);
   std::memset(&out, 0, sizeof(out));
   out.seg_rows[0] = static_cast<int32_t>(S);
-  out.seg_rows[1] = static_cast<int32_t>(ring_rows);
-  out.seg_rows[2] = static_cast<int32_t>(s->lq);
-  const size_t bank_off = static_cast<size_t>(step) * S * row_elems * 2;
+  out.seg_rows[1] = static_cast<int32_t>(c0);
+  out.seg_rows[2] = static_cast<int32_t>(c1);
+  out.seg_rows[3] = static_cast<int32_t>(view.lq);
+  const size_t bank_off = static_cast<size_t>(step) * S * row_bytes;
   if (S > 0) {
     if (!encode_rows(&out.kmap[0], static_cast<const char*>(s->buf.sink_k) + bank_off, S, row_elems) ||
         !encode_rows(&out.vmap[0], static_cast<const char*>(s->buf.sink_v) + bank_off, S, row_elems))
       return SR_ERR_CUDA;
   }
-  if (ring_rows > 0) {
-    if (!encode_rows(&out.kmap[1], s->buf.ring_k, ring_rows, row_elems) ||
-        !encode_rows(&out.vmap[1], s->buf.ring_v, ring_rows, row_elems))
+  if (c0 > 0) {
+    const size_t off = static_cast<size_t>(r0) * row_bytes;
+    if (!encode_rows(&out.kmap[1], static_cast<const char*>(s->buf.ring_k) + off, c0, row_elems) ||
+        !encode_rows(&out.vmap[1], static_cast<const char*>(s->buf.ring_v) + off, c0, row_elems))
       return SR_ERR_CUDA;
   }
-  const char* kc = static_cast<const char*>(k) + static_cast<size_t>(row0) * row_elems * 2;
-  const char* vc = static_cast<const char*>(v) + static_cast<size_t>(row0) * row_elems * 2;
-  if (!encode_rows(&out.kmap[2], kc, s->lq, row_elems) || !encode_rows(&out.vmap[2], vc, s->lq, row_elems))
+  if (c1 > 0) {
+    if (!encode_rows(&out.kmap[2], s->buf.ring_k, c1, row_elems) ||
+        !encode_rows(&out.vmap[2], s->buf.ring_v, c1, row_elems))
+      return SR_ERR_CUDA;
+  }
+  const char* kc = static_cast<const char*>(k) + static_cast<size_t>(row0) * row_bytes;
+  const char* vc = static_cast<const char*>(v) + static_cast<size_t>(row0) * row_bytes;
+  if (!encode_rows(&out.kmap[3], kc, view.lq, row_elems) || !encode_rows(&out.vmap[3], vc, view.lq, row_elems))
     return SR_ERR_CUDA;
   out.q_row0 = static_cast<int32_t>(row0);
-  out.lq = static_cast<int32_t>(s->lq);
-  out.nqb = static_cast<int32_t>((s->lq + 255) / 256);
+  out.lq = static_cast<int32_t>(view.lq);
+  out.nqb = static_cast<int32_t>((view.lq + 255) / 256);
   if (s->buf.workspace) {
     char* ws = static_cast<char*>(s->buf.workspace);
     out.ws_ctr = reinterpret_cast<int32_t*>(ws);
@@ -181,23 +222,18 @@ sr_status fill_session(sr::AttnSession& out, sr_session* s, int step, const void
   return SR_OK;
 }
 
-// Key tiles a session's chunk attends over (sink bank + occupied ring + chunk).
-int64_t key_tiles(const sr_session* s) {
-  const int64_t rows[3] = {s->cfg.n_sink,
-                           std::min<int64_t>(s->n_committed, s->cfg.window_frames) * s->tokens_per_frame, s->lq};
+// Key tiles a session's chunk attends over (sink bank + visible ring + chunk).
+int64_t key_tiles(const sr_session* s, const ChunkView& view) {
+  int64_t r0 = 0, c0 = 0, c1 = 0;
+  ring_ranges(s, view.hist, r0, c0, c1);
+  const int64_t rows[4] = {s->cfg.n_sink, c0, c1, view.lq};
   int64_t n = 0;
   for (int64_t r : rows) n += (r + 127) / 128;
   return n;
 }
 
-// How many CTAs share the key range of each single-tile last block. Units are
-// dispatched in order (full blocks, then last blocks) to whichever SM frees up
-// first, one CTA per SM; estimate that schedule's makespan for 1..4 parts and
-// keep the best. Cost model in key-tile iterations: a full block walks all its
-// key tiles with two query tiles; a last-block part walks its share split over
-// two halves, about 1.35x slower per iteration (two K/V streams), plus a small
-// merge charge.
-int choose_tail_split(sr_session* const* ss, const int* order, int n) {
+// How many CTAs share the key range of each single-tile last block.
+int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* order, int n) {
   // The single-tile last blocks run after every full block (longest first)
   // and land on the few SMs the last wave of full blocks leaves free; cutting
   // their key ranges into parts spreads them over more SMs and shortens the
@@ -211,9 +247,10 @@ int choose_tail_split(sr_session* const* ss, const int* order, int n) {
   int64_t min_kv = INT64_MAX;
   for (int r = 0; r < n; ++r) {
     const sr_session* s = ss[order[r]];
-    const int64_t rem = s->lq % 256;
+    const ChunkView& view = views[order[r]];
+    const int64_t rem = view.lq % 256;
     if (!s->buf.workspace || rem == 0 || rem > 128) return 1;   // no single-tile last block
-    min_kv = std::min(min_kv, key_tiles(s));
+    min_kv = std::min(min_kv, key_tiles(s, view));
   }
   const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, min_kv));
   if (forced > 0) return std::max(1, std::min(forced, cap));
@@ -249,9 +286,10 @@ sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, con
   // the scratch stands in for the session's workspace for this call only
   void* own = s->buf.workspace;
   s->buf.workspace = scratch;
-  sr_status st = fill_session(p.sess[0], s, step, k, v, 0);
+  const ChunkView view = default_view(s);
+  sr_status st = fill_session(p.sess[0], s, view, step, k, v, 0);
   const int order0 = 0;
-  const int split = st == SR_OK ? choose_tail_split(&s, &order0, 1) : 1;
+  const int split = st == SR_OK ? choose_tail_split(&s, &view, &order0, 1) : 1;
   s->buf.workspace = own;
   if (st != SR_OK) return st;
   p.n_full_units = s->cfg.n_heads * (p.sess[0].nqb - 1);
@@ -362,22 +400,37 @@ sr_status sr_session_frames(const sr_session* s, int64_t* n) {
   return SR_OK;
 }
 
-static sr_status rope_common(sr_session* s, const void* a_src, const void* b_src, void* a_dst, void* b_dst,
-                             int mode, void* stream) {
+// Frames a single call may carry: the limits sr_session_init applies to the
+// configured chunk length.
+static bool frames_ok(const sr_session* s, int64_t n_frames) {
+  const int64_t row = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
+  const int64_t limit = int64_t(1) << 30;
+  if (n_frames < 1 || n_frames > limit) return false;
+  const int64_t lq = n_frames * s->tokens_per_frame;
+  return lq <= limit / 4 && lq * row <= limit;
+}
+
+// RoPE (mode 0) or commit (mode 1) of `n_frames` frames; frame f has time
+// t_clock0 + n_committed + f.
+static sr_status rope_common(sr_session* s, int64_t n_frames, const void* a_src, const void* b_src, void* a_dst,
+                             void* b_dst, int mode, void* stream) {
   sr::RopeParams p;
   std::memset(&p, 0, sizeof(p));
-  p.src0 = static_cast<const __nv_bfloat16*>(a_src);
-  p.src1 = static_cast<const __nv_bfloat16*>(b_src);
+  int64_t first = 0;   // first frame of the chunk that is processed
+  if (mode == 1 && n_frames > s->cfg.window_frames) first = n_frames - s->cfg.window_frames;
+  const size_t skip = static_cast<size_t>(first * s->tokens_per_frame) * s->cfg.n_heads * s->cfg.head_dim;
+  p.src0 = static_cast<const __nv_bfloat16*>(a_src) + skip;
+  p.src1 = static_cast<const __nv_bfloat16*>(b_src) + skip;
   p.dst0 = static_cast<__nv_bfloat16*>(a_dst);
   p.dst1 = static_cast<__nv_bfloat16*>(b_dst);
   p.slot_frame = s->buf.slot_frame;
-  p.n_committed = s->n_committed;
-  p.n_tok = static_cast<int32_t>(s->lq);
+  p.n_committed = s->n_committed + first;
+  p.n_tok = static_cast<int32_t>((n_frames - first) * s->tokens_per_frame);
   p.n_heads = s->cfg.n_heads;
   p.tokens_per_frame = static_cast<int32_t>(s->tokens_per_frame);
   p.grid_w = s->cfg.grid_w;
   p.window_frames = s->cfg.window_frames;
-  p.chunk_frames = s->cfg.chunk_frames;
+  p.chunk_frames = static_cast<int32_t>(n_frames - first);
   p.t_clock0 = s->cfg.t_clock0;
   p.mode = mode;
   for (int i = 0; i < 64; ++i) {
@@ -389,34 +442,42 @@ static sr_status rope_common(sr_session* s, const void* a_src, const void* b_src
   return e == cudaSuccess ? SR_OK : SR_ERR_CUDA;
 }
 
-sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream) {
-  if (!s) return SR_ERR_INVALID_ARG;
+sr_status sr_rope3d_qk_frames(sr_session* s, int32_t n_frames, void* q, void* k, void* stream) {
+  if (!s || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
   if ((q && !aligned16(q)) || (k && !aligned16(k))) return SR_ERR_ALIGN;
   if (!q && !k) return SR_OK;
-  // a single tensor: rotate it twice over the same pointer is wrong, so pair
-  // it with itself only through the first operand and a scratch-free no-op
-  if (q && k) return rope_common(s, q, k, q, k, 0, stream);
+  if (q && k) return rope_common(s, n_frames, q, k, q, k, 0, stream);
   // One tensor: pass it as both operands. Each 16-byte vector is loaded by one
   // thread into two registers before either store, so both stores write the
   // same once-rotated value.
   void* x = q ? q : k;
-  return rope_common(s, x, x, x, x, 0, stream);
+  return rope_common(s, n_frames, x, x, x, x, 0, stream);
 }
 
-sr_status sr_cache_commit(sr_session* s, const void* k_raw, const void* v, void* stream) {
-  if (!s || !k_raw || !v) return SR_ERR_INVALID_ARG;
+sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream) {
+  if (!s) return SR_ERR_INVALID_ARG;
+  return sr_rope3d_qk_frames(s, s->cfg.chunk_frames, q, k, stream);
+}
+
+sr_status sr_cache_commit_frames(sr_session* s, int32_t n_frames, const void* k_raw, const void* v, void* stream) {
+  if (!s || !k_raw || !v || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
   if (!aligned16(k_raw) || !aligned16(v)) return SR_ERR_ALIGN;
   if (s->cfg.window_frames == 0) {
-    s->n_committed += s->cfg.chunk_frames;
+    s->n_committed += n_frames;
     return SR_OK;
   }
-  sr_status st = rope_common(s, k_raw, v, s->buf.ring_k, s->buf.ring_v, 1, stream);
-  if (st == SR_OK) s->n_committed += s->cfg.chunk_frames;
+  sr_status st = rope_common(s, n_frames, k_raw, v, s->buf.ring_k, s->buf.ring_v, 1, stream);
+  if (st == SR_OK) s->n_committed += n_frames;
   return st;
 }
 
-sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const void* k, const void* v, void* o,
-                             float* lse, void* stream) {
+sr_status sr_cache_commit(sr_session* s, const void* k_raw, const void* v, void* stream) {
+  if (!s) return SR_ERR_INVALID_ARG;
+  return sr_cache_commit_frames(s, s->cfg.chunk_frames, k_raw, v, stream);
+}
+
+static sr_status attention_view(sr_session* s, const ChunkView& view, int32_t step, const void* q, const void* k,
+                                const void* v, void* o, float* lse, void* stream) {
   if (!s || !q || !k || !v || !o) return SR_ERR_INVALID_ARG;
   if (step < 0 || step >= s->cfg.n_steps) return SR_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -428,8 +489,8 @@ sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const v
   std::memset(p, 0, sizeof(*p));
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
   sr_status st = SR_OK;
-  if (!encode_rows(&p->qmap, q, s->lq, row_elems)) st = SR_ERR_CUDA;
-  if (st == SR_OK) st = fill_session(p->sess[0], s, step, k, v, 0);
+  if (!encode_rows(&p->qmap, q, view.lq, row_elems)) st = SR_ERR_CUDA;
+  if (st == SR_OK) st = fill_session(p->sess[0], s, view, step, k, v, 0);
   int n_units = 0;
   if (st == SR_OK) {
     // full 256-row blocks first (longest units), then the last block of every head
@@ -437,12 +498,12 @@ sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const v
     p->sess[0].tail_begin = 0;
     p->n_full_units = s->cfg.n_heads * (p->sess[0].nqb - 1);
     const int order0 = 0;
-    p->tail_split = choose_tail_split(&s, &order0, 1);
+    p->tail_split = choose_tail_split(&s, &view, &order0, 1);
     n_units = p->n_full_units + s->cfg.n_heads * p->tail_split;
     p->n_sess = 1;
     p->n_heads = s->cfg.n_heads;
     p->scale_log2 = s->scale * 1.4426950408889634f;
-    p->lse_ld = lse ? static_cast<int32_t>(s->lq) : 0;
+    p->lse_ld = lse ? static_cast<int32_t>(view.lq) : 0;
     p->o = static_cast<__nv_bfloat16*>(o);
     p->lse = lse;
     p->err_word = s->buf.err_word;
@@ -452,6 +513,22 @@ sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const v
   }
   delete p;
   return st;
+}
+
+sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const void* k, const void* v, void* o,
+                             float* lse, void* stream) {
+  if (!s) return SR_ERR_INVALID_ARG;
+  return attention_view(s, default_view(s), step, q, k, v, o, lse, stream);
+}
+
+sr_status sr_chunk_attention_frames(sr_session* s, int32_t step, int32_t n_frames, int32_t hist_frames,
+                                    const void* q, const void* k, const void* v, void* o, float* lse,
+                                    void* stream) {
+  if (!s || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
+  const int64_t occupied = std::min<int64_t>(s->n_committed, s->cfg.window_frames);
+  if (hist_frames < -1 || hist_frames > occupied) return SR_ERR_INVALID_ARG;
+  const ChunkView view{n_frames * s->tokens_per_frame, hist_frames == -1 ? occupied : hist_frames};
+  return attention_view(s, view, step, q, k, v, o, lse, stream);
 }
 
 sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32_t step, const void* q,
@@ -480,6 +557,8 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
     return s->cfg.n_sink + std::min<int64_t>(s->n_committed, s->cfg.window_frames) * s->tokens_per_frame + s->lq;
   };
   std::stable_sort(order, order + n, [&](int a, int b) { return lk(a) > lk(b); });
+  ChunkView views[SR_MAX_BATCH];
+  for (int i = 0; i < n; ++i) views[i] = default_view(sessions[i]);
 
   if (ensure_attn_attr(s0->cfg.head_dim, sr::kAttnMaxBatch) != cudaSuccess) return SR_ERR_CUDA;
   auto* p = new (std::nothrow) sr::AttnParams<sr::kAttnMaxBatch>;
@@ -493,13 +572,13 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
   int full = 0, tails = 0;
   for (int r = 0; st == SR_OK && r < n; ++r) {
     const int i = order[r];
-    st = fill_session(p->sess[r], sessions[i], step, k, v, q_off[i]);
+    st = fill_session(p->sess[r], sessions[i], views[i], step, k, v, q_off[i]);
     p->sess[r].unit_begin = full;
     p->sess[r].tail_begin = tails;
     full += s0->cfg.n_heads * (p->sess[r].nqb - 1);
     tails += s0->cfg.n_heads;
   }
-  const int split = st == SR_OK ? choose_tail_split(sessions, order, n) : 1;
+  const int split = st == SR_OK ? choose_tail_split(sessions, views, order, n) : 1;
   const int units = full + tails * split;
   if (st == SR_OK) {
     p->n_full_units = full;
@@ -517,6 +596,40 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
   }
   delete p;
   return st;
+}
+
+// The unit rhythm of the teardown's shipped configuration: latents come in
+// codec groups of five (the first covers one RGB frame, the others four);
+// merging that one-frame latent into its neighbour makes units of 2, 1, 1, 1
+// latents. Chunk 0 is the first window (bootstrap_units units, no history);
+// chunk c >= 1 is chunk_units units and sees the window_units units before it.
+static int64_t latents_before(int64_t u, bool merge) {   // latents in units 0 .. u-1
+  if (!merge) return u;
+  return u + (u + 3) / 4;   // units 0, 4, 8, ... below u hold one latent more
+}
+
+sr_status sr_plan_chunk(int32_t c, int32_t bootstrap_units, int32_t chunk_units, int32_t window_units,
+                        int32_t sink_units, int32_t merge_single_frame_units, sr_chunk_plan* out) {
+  if (!out || c < 0 || bootstrap_units < 1 || chunk_units < 1 || window_units < 0 || sink_units < 0)
+    return SR_ERR_INVALID_ARG;
+  const bool m = merge_single_frame_units != 0;
+  const int64_t u0 = c == 0 ? 0 : bootstrap_units + static_cast<int64_t>(c - 1) * chunk_units;
+  const int64_t nu = c == 0 ? bootstrap_units : chunk_units;
+  const int64_t first = latents_before(u0, m);
+  const int64_t n = latents_before(u0 + nu, m) - first;
+  int64_t hist = 0;
+  if (c > 0) {
+    const int64_t hu = std::min<int64_t>(window_units, u0);
+    hist = first - latents_before(u0 - hu, m);
+  }
+  const int64_t sink = latents_before(sink_units, m);
+  const int64_t lim = INT32_MAX;
+  if (first + n > lim || sink > lim) return SR_ERR_INVALID_ARG;
+  out->first_frame = static_cast<int32_t>(first);
+  out->n_frames = static_cast<int32_t>(n);
+  out->hist_frames = static_cast<int32_t>(hist);
+  out->sink_frames = static_cast<int32_t>(sink);
+  return SR_OK;
 }
 
 sr_status sr_session_free(sr_session* s) {

@@ -12,14 +12,17 @@
 namespace sr {
 
 // ------------------------------------------------------------ attention
-// One session's view for one launch: three key/value segments (sink bank of
-// the step, occupied ring prefix, the chunk itself), each a 2D tensor map over
-// [rows][H*d] bf16 with a {64, 128} box and 128-byte swizzle. A segment with
-// zero rows has no map and contributes no tiles.
+// One session's view for one launch: up to four key/value segments -- the sink
+// bank of the step, the visible ring frames as one or two contiguous row
+// ranges (two when a history window wraps around the end of the ring), and
+// the chunk itself -- each a 2D tensor map over [rows][H*d] bf16 with a
+// {64, 128} box and 128-byte swizzle. A segment with zero rows has no map and
+// contributes no tiles.
+constexpr int kSegs = 4;
 struct alignas(128) AttnSession {
-  CUtensorMap kmap[3];
-  CUtensorMap vmap[3];
-  int32_t seg_rows[3];
+  CUtensorMap kmap[kSegs];
+  CUtensorMap vmap[kSegs];
+  int32_t seg_rows[kSegs];
   int32_t q_row0;       // first row of this session in the packed q / o
   int32_t lq;           // query rows
   int32_t nqb;          // query blocks of 256 rows

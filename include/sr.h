@@ -207,6 +207,52 @@ SR_API sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n
 SR_API sr_status sr_chunk_attention_noalloc(sr_session* s, int32_t step, const void* q, const void* k,
                                             const void* v, void* o, float* lse, void* stream);
 
+/*
+ * The pages' unit rhythm ([teardown] "A window that slides, and a prefix that
+ * doesn't"; [H3 page] 3.1.2). The video codec turns 17 RGB frames into 5 latent
+ * frames, the first of every five covering one RGB frame; with single-frame latents
+ * merged into their neighbour, scheduling units hold 2, 1, 1, 1 latents and repeat.
+ * A stream opens with one window of bootstrap_units units, then every chunk is
+ * chunk_units units and sees the window_units units right before it as recent
+ * history; the sink is the first sink_units units. With the shipped values (7, 2,
+ * 2, 2, merged) the first window is 9 latents and the chunks alternate 3 and 2
+ * latents with 2 and 3 latents of history.
+ * Host-only arithmetic (no GPU call): fills *out for chunk `chunk_index` (0 = the
+ * first window, which has no history). Invalid (non-positive unit counts, negative
+ * index, sums past int32): SR_ERR_INVALID_ARG.
+ */
+typedef struct {
+  int32_t first_frame;   /* stream index of the chunk's first latent frame */
+  int32_t n_frames;      /* latent frames in the chunk */
+  int32_t hist_frames;   /* latent frames of recent history the chunk sees */
+  int32_t sink_frames;   /* latent frames in the sink units */
+} sr_chunk_plan;
+SR_API sr_status sr_plan_chunk(int32_t chunk_index, int32_t bootstrap_units, int32_t chunk_units,
+                               int32_t window_units, int32_t sink_units, int32_t merge_single_frame_units,
+                               sr_chunk_plan* out);
+
+/*
+ * The per-chunk calls for chunks of any length (the unit rhythm above).
+ * n_frames: latent frames in this chunk, 1 <= n_frames and n_frames*T*H*d within the
+ * limits sr_session_init applies to chunk_frames (sr_config.chunk_frames is the
+ * length the plain calls use). q, k, v, o, k_raw: [n_frames*T][H][d] bf16.
+ * - sr_rope3d_qk_frames: as sr_rope3d_qk, frames n .. n+n_frames-1.
+ * - sr_chunk_attention_frames: as sr_chunk_attention over sink bank[step] U the last
+ *   hist_frames committed frames U the chunk; hist_frames = -1 means every occupied
+ *   slot (what sr_chunk_attention sees), otherwise 0 <= hist_frames <= min(n, W).
+ *   The visible frames may wrap around the end of the ring. lse: [H][n_frames*T].
+ * - sr_cache_commit_frames: as sr_cache_commit for n_frames frames, which may wrap
+ *   around the end of the ring; when n_frames > W only the chunk's last W frames
+ *   are written (its earlier frames would be evicted by its later ones), and n
+ *   still advances by n_frames.
+ */
+SR_API sr_status sr_rope3d_qk_frames(sr_session* s, int32_t n_frames, void* q, void* k, void* stream);
+SR_API sr_status sr_chunk_attention_frames(sr_session* s, int32_t step, int32_t n_frames, int32_t hist_frames,
+                                           const void* q, const void* k, const void* v, void* o, float* lse,
+                                           void* stream);
+SR_API sr_status sr_cache_commit_frames(sr_session* s, int32_t n_frames, const void* k_raw, const void* v,
+                                        void* stream);
+
 /* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
 SR_API sr_status sr_device_error_status(int32_t err_word_value);
 

@@ -118,8 +118,10 @@ def session_sinks(shape: Shape, config: int, session: int = 0, base_seed: int = 
 
 
 def chunk_inputs(shape: Shape, config: int, session: int = 0, chunk: int = 0,
-                 base_seed: int = 0, q_scale: float = 1.0) -> ChunkInputs:
-    dims = (shape.lq, shape.n_heads, shape.head_dim)
+                 base_seed: int = 0, q_scale: float = 1.0, frames: int | None = None) -> ChunkInputs:
+    """Inputs of one chunk of ``frames`` latent frames (default: the shape's chunk length)."""
+    rows = shape.lq if frames is None else frames * shape.tokens_per_frame
+    dims = (rows, shape.n_heads, shape.head_dim)
     q, k, v = [], [], []
     for s in range(shape.n_steps):
         q.append(normal_bf16_bits(dims, rng(config, session, chunk, s, T_Q, base_seed), q_scale))
