@@ -24,7 +24,8 @@ What it computes, and where the pages define it. The pages are
 * ``session``    one static sink bank per denoising step ([H3-page] 3.3
   "Static-context KV caching"; [teardown] "A window that slides, and a prefix
   that doesn't"), two steps then commit; chunks of any number of frames and
-  a recent history of the last h committed frames.
+  a recent history of the last h committed frames; the page-faithful window
+  (prefix rows see only the prefix, recomputed moving rows see everything).
 * ``schedule``   the scheduling units (2, 1, 1, 1 latents), the 7-unit first
   window and the per-chunk plan ([teardown] "A window that slides, and a
   prefix that doesn't"; [H3-page] 3.1.2).

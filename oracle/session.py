@@ -71,6 +71,36 @@ class OracleSession:
         k = rope3d(bf16_bits_to_f64(k_bits), t, h, w, self.base)
         return f64_to_bf16_bits(q), f64_to_bf16_bits(k)
 
+    def rope3d_at(self, first_frame, frames, q_bits, k_bits):
+        """Rotate the rows of ``frames`` consecutive frames whose first frame is
+        the stream's frame ``first_frame`` (time t_clock0 + first_frame + f):
+        used for recomputed history rows, which keep their own frame times."""
+        t, h, w = token_positions(frames * self.T, self.grid_h, self.grid_w, self.t_clock0 + first_frame)
+        q = rope3d(bf16_bits_to_f64(q_bits), t, h, w, self.base)
+        k = rope3d(bf16_bits_to_f64(k_bits), t, h, w, self.base)
+        return f64_to_bf16_bits(q), f64_to_bf16_bits(k)
+
+    def window_attention(self, step, q_bits, k_moving_bits, v_moving_bits, with_prefix):
+        """The pages' window with a fixed prefix and a moving part ([teardown]
+        "A window that slides, and a prefix that doesn't"; [H3-page] 3.1.2
+        "Prefix cache"): the prefix rows attend only to the prefix, the moving
+        rows (recomputed recent history, then the chunk) attend to the whole
+        window. The prefix's keys and values are the bank of the step.
+        q: [S + M][H][d] with the S prefix rows first when ``with_prefix``,
+        else [M][H][d]; k_moving, v_moving: [M][H][d]. Returns (o, lse) for
+        the rows of q, in order."""
+        if not 0 <= step < self.n_steps:
+            raise ValueError("step out of range")
+        S = self.S if with_prefix else 0
+        q = bf16_bits_to_f64(q_bits)
+        km, vm = bf16_bits_to_f64(k_moving_bits), bf16_bits_to_f64(v_moving_bits)
+        kp, vp = self.sink_k[step], self.sink_v[step]
+        o_m, l_m = attention(q[S:], np.concatenate([kp, km]), np.concatenate([vp, vm]), self.scale)
+        if not with_prefix:
+            return o_m, l_m
+        o_p, l_p = attention(q[:S], kp, vp, self.scale)
+        return np.concatenate([o_p, o_m]), np.concatenate([l_p, l_m], axis=1)
+
     def visible_kv(self, step, k_bits, v_bits, hist=None):
         """bank[step], then the ring's frames (every occupied slot, or only
         the last ``hist`` committed frames), then the chunk."""
