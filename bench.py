@@ -9,10 +9,12 @@ used alternately, so every step reads inputs that were last touched more
 than an L2's worth of traffic ago.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2|3]
-                    [--workload steady|rhythm]
+                    [--workload steady|rhythm|window]
 
 ``--workload rhythm`` times the pages' unit rhythm instead (chunks of 3 and 2
-latent frames at the 832x480 frame size) and prints its own line.
+latent frames at the 832x480 frame size) and ``--workload window`` the
+page-faithful window (recomputed history rows as queries); each prints its own
+line.
 
 Multi-GPU: the path has no exchange step, so N ranks run N independent
 replicas (weak scaling, no collective on the data path); rank 0 prints the
@@ -509,6 +511,106 @@ def run_rhythm(args):
     print(json.dumps(out), flush=True)
 
 
+def run_window(args):
+    """The page-faithful window at the 832x480 frame size under the unit rhythm:
+    every chunk recomputes its moving rows (2 or 3 latents of history, then the
+    3- or 2-latent chunk: 5 latent frames, 7800 rows) and attends them over the
+    bank of the step and themselves; the prefix pass (2072 prefix rows over
+    the bank alone) runs in the same launch on the first window only and is
+    timed separately. One bench step = one chunk: 2 x (RoPE at the moving rows'
+    frame times + window attention). No ring: this is what the ring caches."""
+    import chunked_kv_cache_gb300 as sr
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_kv_cache_gb300 import build
+    build.build()
+    base = syn.SHAPES[2]
+    T, H, d, S = base.tokens_per_frame, base.n_heads, base.head_dim, base.n_sink
+    moving = 5
+    M = moving * T
+    sessions = []
+    for sid in range(2):
+        sink = lambda tid: syn.device_normal_bf16((base.n_steps, S, H, d), dev, 6, sid, 0, 0, tid)
+        s = sr.Session(H, d, base.grid_h, base.grid_w, 3, 0, S, base.n_steps, sink_k=sink(syn.T_SINK_K),
+                       sink_v=sink(syn.T_SINK_V), workspace=False, device=dev)
+        x = {k: [syn.device_normal_bf16((M, H, d), dev, 6, sid, 1, st, tid) for st in range(base.n_steps)]
+             for k, tid in (("q", syn.T_Q), ("k", syn.T_K), ("v", syn.T_V))}
+        x["o"] = torch.empty((M, H, d), dtype=torch.bfloat16, device=dev)
+        x["qp"] = syn.device_normal_bf16((S + M, H, d), dev, 6, sid, 2, 0, syn.T_Q)
+        x["op"] = torch.empty_like(x["qp"])
+        sessions.append((s, x))
+    first = [9]
+
+    def chunk(s, x, c, ev=None):
+        plan = sr.plan_chunk(c)
+        h, F = plan["hist_frames"], plan["n_frames"]
+        assert h + F == moving
+        for st in range(base.n_steps):
+            s.rope3d_at(plan["first_frame"] - h, moving, x["q"][st], x["k"][st])
+            if ev is not None:
+                ev[st][0].record()
+            s.window_attention(st, x["q"][st], x["k"][st], x["v"][st], moving, out=x["o"])
+            if ev is not None:
+                ev[st][1].record()
+
+    for i in range(max(args.warmup, 3)):
+        chunk(*sessions[i % 2], 1 + i)
+    torch.cuda.synchronize()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [[mk() for _ in range(base.n_steps)] for _ in range(args.steps)]
+    t0, t1 = mk()
+    with Clocks(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        t0.record()
+        for i in range(args.steps):
+            chunk(*sessions[i % 2], 1 + i, evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+    # the prefix pass of a first window: prefix and moving rows in one launch
+    pe = mk()
+    s, x = sessions[0]
+    for _ in range(3):
+        s.window_attention(0, x["qp"], x["k"][0], x["v"][0], moving, with_prefix=True, out=x["op"])
+    torch.cuda.synchronize()
+    pe[0].record()
+    s.window_attention(0, x["qp"], x["k"][0], x["v"][0], moving, with_prefix=True, out=x["op"])
+    pe[1].record()
+    torch.cuda.synchronize()
+    for s, _ in sessions:
+        if s.error_status() != 0:
+            raise RuntimeError("device error word set during the bench")
+    elapsed = t0.elapsed_time(t1) / 1e3
+    attn_ms = statistics.mean(a.elapsed_time(b) for ev in evs for a, b in ev)
+    fl = 4.0 * H * M * (S + M) * d
+    fl_pre = fl + 4.0 * H * S * S * d
+    achieved = fl / (attn_ms / 1e3) / 1e12
+    peak_tf, _, peak_kind = _peaks()
+    pre_ms = pe[0].elapsed_time(pe[1])
+    out = {
+        "metric": "page-faithful window attention TFLOP/s and ms per chunk on 1 GB300", "value": round(achieved, 2),
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_chunk": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "832x480 latent frames (24x128, 30x52 grid, S=2072 prefix rows), the pages' "
+                               "window: per chunk 5 latent frames of moving rows (recomputed history + chunk, "
+                               "7800 rows) over the bank and themselves; one step = one chunk: 2 x (RoPE at the "
+                               "rows' frame times + window attention)",
+                   "lq": M, "lk": S + M, "l2": "two sessions used alternately"},
+        "attention_ms_per_denoise_step": round(attn_ms, 4),
+        "prefix_pass": {"ms": round(pre_ms, 4), "rows": S + M,
+                        "tflops": round(fl_pre / (pre_ms / 1e3) / 1e12, 2),
+                        "what": "first window: 2072 prefix rows over the bank alone + 7800 moving rows, one launch"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4), "kernel": "attn_kernel (sr_window_attention)",
+                     "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "clocks": clk.summary(),
+        "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,8 +618,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, choices=[2, 3], default=2)
-    ap.add_argument("--workload", choices=["steady", "rhythm"], default="steady",
-                    help="steady: the headline chunk workload; rhythm: the pages' 3/2-latent unit rhythm")
+    ap.add_argument("--workload", choices=["steady", "rhythm", "window"], default="steady",
+                    help="steady: the headline chunk workload; rhythm: the pages' 3/2-latent unit rhythm; "
+                         "window: the page-faithful window (recomputed history rows as queries)")
     ap.add_argument("--profile", action="store_true",
                     help="under a profiler: skip the end-to-end and CPU-baseline legs (their numbers are not reported)")
     args = ap.parse_args()
@@ -527,6 +630,8 @@ def main():
         run_reference(args)
     elif args.workload == "rhythm":
         run_rhythm(args)
+    elif args.workload == "window":
+        run_window(args)
     else:
         run_ours(args)
 

@@ -15,7 +15,7 @@ from ._native import (SrConfig, SrBuffers, SrError, sr_session_init, sr_session_
                       sr_rope3d_qk, sr_chunk_attention, sr_cache_commit, sr_session_free,
                       sr_chunk_attention_batch, sr_device_error_status, sr_debug_wait_timeout,
                       sr_workspace_bytes, sr_plan_chunk, sr_rope3d_qk_frames, sr_chunk_attention_frames,
-                      sr_cache_commit_frames, SrChunkPlan, SR_MAX_BATCH)
+                      sr_cache_commit_frames, SrChunkPlan, sr_window_attention, sr_rope3d_qk_at, SR_MAX_BATCH)
 
 __all__ = [
     "Session", "chunk_attention_batch", "SrConfig", "SrBuffers", "SrError",
@@ -23,6 +23,7 @@ __all__ = [
     "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch", "sr_device_error_status",
     "sr_debug_wait_timeout", "sr_workspace_bytes", "sr_plan_chunk", "sr_rope3d_qk_frames",
     "sr_chunk_attention_frames", "sr_cache_commit_frames", "SrChunkPlan", "plan_chunk",
+    "sr_window_attention", "sr_rope3d_qk_at",
 ]
 
 _BF16 = torch.bfloat16
@@ -149,6 +150,37 @@ class Session:
             sr_cache_commit(self.handle, k.data_ptr(), v.data_ptr(), _stream(self.device))
         else:
             sr_cache_commit_frames(self.handle, frames, k.data_ptr(), v.data_ptr(), _stream(self.device))
+
+    # ------------------------------------------------ the page-faithful window
+    def rope3d_at(self, first_frame: int, frames: int, q: torch.Tensor | None, k: torch.Tensor | None) -> None:
+        """RoPE on rows of `frames` frames starting at the stream's frame `first_frame`."""
+        for name, t in (("q", q), ("k", k)):
+            if t is not None:
+                self._chunk(name, t, frames)
+        sr_rope3d_qk_at(self.handle, first_frame, frames, _ptr(q), _ptr(k), _stream(self.device))
+
+    def window_attention(self, step: int, q: torch.Tensor, k_moving: torch.Tensor, v_moving: torch.Tensor,
+                         moving_frames: int, with_prefix: bool = False, out: torch.Tensor | None = None,
+                         lse: torch.Tensor | bool | None = None):
+        """Prefix rows (first n_sink rows of q when with_prefix) see the bank only;
+        moving rows see the bank and k_moving / v_moving."""
+        M = moving_frames * self.T
+        P = self.S if with_prefix else 0
+        _check_tensor("q", q, (P + M, self.H, self.d), self.device)
+        _check_tensor("k_moving", k_moving, (M, self.H, self.d), self.device)
+        _check_tensor("v_moving", v_moving, (M, self.H, self.d), self.device)
+        if out is None:
+            out = torch.empty_like(q)
+        _check_tensor("out", out, (P + M, self.H, self.d), self.device)
+        if lse is True:
+            lse = torch.empty((self.H, P + M), dtype=torch.float32, device=self.device)
+        if isinstance(lse, torch.Tensor):
+            _check_tensor("lse", lse, (self.H, P + M), self.device, torch.float32)
+        else:
+            lse = None
+        sr_window_attention(self.handle, step, moving_frames, with_prefix, q.data_ptr(), k_moving.data_ptr(),
+                            v_moving.data_ptr(), out.data_ptr(), _ptr(lse), _stream(self.device))
+        return (out, lse) if lse is not None else out
 
     def close(self) -> None:
         if self.handle is not None:

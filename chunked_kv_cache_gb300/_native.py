@@ -28,7 +28,7 @@ EXPORTS = (
     "sr_chunk_attention", "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch",
     "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string", "sr_workspace_bytes",
     "sr_chunk_attention_noalloc", "sr_plan_chunk", "sr_rope3d_qk_frames", "sr_chunk_attention_frames",
-    "sr_cache_commit_frames",
+    "sr_cache_commit_frames", "sr_window_attention", "sr_rope3d_qk_at",
 )
 
 
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.sr_rope3d_qk_frames.argtypes = [vp, i32, vp, vp, vp]
         L.sr_chunk_attention_frames.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.sr_cache_commit_frames.argtypes = [vp, i32, vp, vp, vp]
+        L.sr_window_attention.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.sr_rope3d_qk_at.argtypes = [vp, i64, i32, vp, vp, vp]
         L.sr_chunk_attention_batch.argtypes = [ctypes.POINTER(vp), i32, i32, vp, vp, vp,
                                                ctypes.POINTER(i64), vp, vp, vp]
         L.sr_device_error_status.argtypes = [i32]
@@ -168,6 +170,17 @@ def sr_chunk_attention_frames(handle: int, step: int, n_frames: int, hist_frames
 
 def sr_cache_commit_frames(handle: int, n_frames: int, k_raw: int, v: int, stream: int) -> None:
     _check(lib().sr_cache_commit_frames(handle, int(n_frames), k_raw, v, stream or None), "sr_cache_commit_frames")
+
+
+def sr_window_attention(handle: int, step: int, moving_frames: int, with_prefix: bool, q: int, k_moving: int,
+                        v_moving: int, o: int, lse: int, stream: int) -> None:
+    _check(lib().sr_window_attention(handle, int(step), int(moving_frames), 1 if with_prefix else 0, q, k_moving,
+                                     v_moving, o, lse or None, stream or None), "sr_window_attention")
+
+
+def sr_rope3d_qk_at(handle: int, first_frame: int, n_frames: int, q: int, k: int, stream: int) -> None:
+    _check(lib().sr_rope3d_qk_at(handle, int(first_frame), int(n_frames), q or None, k or None, stream or None),
+           "sr_rope3d_qk_at")
 
 
 def sr_chunk_attention_noalloc(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int,

@@ -173,44 +173,52 @@ void ring_ranges(const sr_session* s, int64_t hist, int64_t& r0, int64_t& c0, in
   }
 }
 
+// One key/value segment of a query group: rows [0, rows) of the buffers k, v.
+struct Segment {
+  const void* k;
+  const void* v;
+  int64_t rows;
+};
+
+// Encode a query group's four key/value segments (empty ones get no map),
+// and its query rows [row0, row0 + lq) of the packed q / o.
+sr_status encode_group(sr::AttnSession& out, const Segment (&seg)[sr::kSegs], int64_t row_elems, int64_t row0,
+                       int64_t lq) {
+  std::memset(&out, 0, sizeof(out));
+  for (int i = 0; i < sr::kSegs; ++i) {
+    out.seg_rows[i] = static_cast<int32_t>(seg[i].rows);
+    if (seg[i].rows > 0 && (!encode_rows(&out.kmap[i], seg[i].k, seg[i].rows, row_elems) ||
+                            !encode_rows(&out.vmap[i], seg[i].v, seg[i].rows, row_elems)))
+      return SR_ERR_CUDA;
+  }
+  out.q_row0 = static_cast<int32_t>(row0);
+  out.lq = static_cast<int32_t>(lq);
+  out.nqb = static_cast<int32_t>((lq + 255) / 256);
+  return SR_OK;
+}
+
+const char* bank_ptr(const void* bank, const sr_session* s, int step) {
+  const size_t row_bytes = static_cast<size_t>(s->cfg.n_heads) * s->cfg.head_dim * 2;
+  return static_cast<const char*>(bank) + static_cast<size_t>(step) * s->cfg.n_sink * row_bytes;
+}
+
 // Fill one session's segment maps for `step` (rows of the chunk taken from
 // k, v at row offset `row0` of a packed tensor).
 sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& view, int step, const void* k,
                        const void* v, int64_t row0) {
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
   const size_t row_bytes = static_cast<size_t>(row_elems) * 2;
-  const int64_t S = s->cfg.n_sink;
   int64_t r0 = 0, c0 = 0, c1 = 0;
   ring_ranges(s, view.hist, r0, c0, c1);
-  std::memset(&out, 0, sizeof(out));
-  out.seg_rows[0] = static_cast<int32_t>(S);
-  out.seg_rows[1] = static_cast<int32_t>(c0);
-  out.seg_rows[2] = static_cast<int32_t>(c1);
-  out.seg_rows[3] = static_cast<int32_t>(view.lq);
-  const size_t bank_off = static_cast<size_t>(step) * S * row_bytes;
-  if (S > 0) {
-    if (!encode_rows(&out.kmap[0], static_cast<const char*>(s->buf.sink_k) + bank_off, S, row_elems) ||
-        !encode_rows(&out.vmap[0], static_cast<const char*>(s->buf.sink_v) + bank_off, S, row_elems))
-      return SR_ERR_CUDA;
-  }
-  if (c0 > 0) {
-    const size_t off = static_cast<size_t>(r0) * row_bytes;
-    if (!encode_rows(&out.kmap[1], static_cast<const char*>(s->buf.ring_k) + off, c0, row_elems) ||
-        !encode_rows(&out.vmap[1], static_cast<const char*>(s->buf.ring_v) + off, c0, row_elems))
-      return SR_ERR_CUDA;
-  }
-  if (c1 > 0) {
-    if (!encode_rows(&out.kmap[2], s->buf.ring_k, c1, row_elems) ||
-        !encode_rows(&out.vmap[2], s->buf.ring_v, c1, row_elems))
-      return SR_ERR_CUDA;
-  }
-  const char* kc = static_cast<const char*>(k) + static_cast<size_t>(row0) * row_bytes;
-  const char* vc = static_cast<const char*>(v) + static_cast<size_t>(row0) * row_bytes;
-  if (!encode_rows(&out.kmap[3], kc, view.lq, row_elems) || !encode_rows(&out.vmap[3], vc, view.lq, row_elems))
-    return SR_ERR_CUDA;
-  out.q_row0 = static_cast<int32_t>(row0);
-  out.lq = static_cast<int32_t>(view.lq);
-  out.nqb = static_cast<int32_t>((view.lq + 255) / 256);
+  const size_t ring_off = static_cast<size_t>(r0) * row_bytes;
+  const Segment seg[sr::kSegs] = {
+      {bank_ptr(s->buf.sink_k, s, step), bank_ptr(s->buf.sink_v, s, step), s->cfg.n_sink},
+      {static_cast<const char*>(s->buf.ring_k) + ring_off, static_cast<const char*>(s->buf.ring_v) + ring_off, c0},
+      {s->buf.ring_k, s->buf.ring_v, c1},
+      {static_cast<const char*>(k) + static_cast<size_t>(row0) * row_bytes,
+       static_cast<const char*>(v) + static_cast<size_t>(row0) * row_bytes, view.lq}};
+  sr_status st = encode_group(out, seg, row_elems, row0, view.lq);
+  if (st != SR_OK) return st;
   if (s->buf.workspace) {
     char* ws = static_cast<char*>(s->buf.workspace);
     out.ws_ctr = reinterpret_cast<int32_t*>(ws);
@@ -410,10 +418,11 @@ static bool frames_ok(const sr_session* s, int64_t n_frames) {
   return lq <= limit / 4 && lq * row <= limit;
 }
 
-// RoPE (mode 0) or commit (mode 1) of `n_frames` frames; frame f has time
-// t_clock0 + n_committed + f.
-static sr_status rope_common(sr_session* s, int64_t n_frames, const void* a_src, const void* b_src, void* a_dst,
-                             void* b_dst, int mode, void* stream) {
+// RoPE (mode 0) or commit (mode 1) of `n_frames` frames; frame f is the
+// stream's frame first_frame + f, with time t_clock0 + first_frame + f (the
+// chunk calls pass n_committed).
+static sr_status rope_common(sr_session* s, int64_t first_frame, int64_t n_frames, const void* a_src,
+                             const void* b_src, void* a_dst, void* b_dst, int mode, void* stream) {
   sr::RopeParams p;
   std::memset(&p, 0, sizeof(p));
   int64_t first = 0;   // first frame of the chunk that is processed
@@ -424,7 +433,7 @@ static sr_status rope_common(sr_session* s, int64_t n_frames, const void* a_src,
   p.dst0 = static_cast<__nv_bfloat16*>(a_dst);
   p.dst1 = static_cast<__nv_bfloat16*>(b_dst);
   p.slot_frame = s->buf.slot_frame;
-  p.n_committed = s->n_committed + first;
+  p.n_committed = first_frame + first;
   p.n_tok = static_cast<int32_t>((n_frames - first) * s->tokens_per_frame);
   p.n_heads = s->cfg.n_heads;
   p.tokens_per_frame = static_cast<int32_t>(s->tokens_per_frame);
@@ -446,12 +455,22 @@ sr_status sr_rope3d_qk_frames(sr_session* s, int32_t n_frames, void* q, void* k,
   if (!s || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
   if ((q && !aligned16(q)) || (k && !aligned16(k))) return SR_ERR_ALIGN;
   if (!q && !k) return SR_OK;
-  if (q && k) return rope_common(s, n_frames, q, k, q, k, 0, stream);
+  if (q && k) return rope_common(s, s->n_committed, n_frames, q, k, q, k, 0, stream);
   // One tensor: pass it as both operands. Each 16-byte vector is loaded by one
   // thread into two registers before either store, so both stores write the
   // same once-rotated value.
   void* x = q ? q : k;
-  return rope_common(s, n_frames, x, x, x, x, 0, stream);
+  return rope_common(s, s->n_committed, n_frames, x, x, x, x, 0, stream);
+}
+
+sr_status sr_rope3d_qk_at(sr_session* s, int64_t first_frame, int32_t n_frames, void* q, void* k, void* stream) {
+  if (!s || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
+  if (first_frame < -(int64_t(1) << 40) || first_frame > (int64_t(1) << 40)) return SR_ERR_INVALID_ARG;
+  if ((q && !aligned16(q)) || (k && !aligned16(k))) return SR_ERR_ALIGN;
+  if (!q && !k) return SR_OK;
+  if (q && k) return rope_common(s, first_frame, n_frames, q, k, q, k, 0, stream);
+  void* x = q ? q : k;
+  return rope_common(s, first_frame, n_frames, x, x, x, x, 0, stream);
 }
 
 sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream) {
@@ -466,7 +485,7 @@ sr_status sr_cache_commit_frames(sr_session* s, int32_t n_frames, const void* k_
     s->n_committed += n_frames;
     return SR_OK;
   }
-  sr_status st = rope_common(s, n_frames, k_raw, v, s->buf.ring_k, s->buf.ring_v, 1, stream);
+  sr_status st = rope_common(s, s->n_committed, n_frames, k_raw, v, s->buf.ring_k, s->buf.ring_v, 1, stream);
   if (st == SR_OK) s->n_committed += n_frames;
   return st;
 }
@@ -529,6 +548,61 @@ sr_status sr_chunk_attention_frames(sr_session* s, int32_t step, int32_t n_frame
   if (hist_frames < -1 || hist_frames > occupied) return SR_ERR_INVALID_ARG;
   const ChunkView view{n_frames * s->tokens_per_frame, hist_frames == -1 ? occupied : hist_frames};
   return attention_view(s, view, step, q, k, v, o, lse, stream);
+}
+
+sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames, int32_t with_prefix,
+                              const void* q, const void* k_moving, const void* v_moving, void* o, float* lse,
+                              void* stream) {
+  if (!s || !q || !k_moving || !v_moving || !o || !frames_ok(s, moving_frames)) return SR_ERR_INVALID_ARG;
+  if (step < 0 || step >= s->cfg.n_steps) return SR_ERR_INVALID_ARG;
+  if (with_prefix && s->cfg.n_sink == 0) return SR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_moving) || !aligned16(v_moving) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return SR_ERR_ALIGN;
+  const int64_t P = with_prefix ? s->cfg.n_sink : 0;
+  const int64_t M = static_cast<int64_t>(moving_frames) * s->tokens_per_frame;
+  const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
+  if ((P + M) * row_elems > (int64_t(1) << 31) || P + M > (int64_t(1) << 28)) return SR_ERR_INVALID_ARG;
+  if (ensure_attn_attr(s->cfg.head_dim, sr::kAttnMaxBatch) != cudaSuccess) return SR_ERR_CUDA;
+  auto* p = new (std::nothrow) sr::AttnParams<sr::kAttnMaxBatch>;
+  if (!p) return SR_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  sr_status st = SR_OK;
+  if (!encode_rows(&p->qmap, q, P + M, row_elems)) st = SR_ERR_CUDA;
+  // Two query groups in one launch. Moving rows (longest key range first):
+  // the bank of the step and the moving rows themselves. Prefix rows: the
+  // bank alone -- the asymmetric mask as a choice of key set.
+  const char* bk = bank_ptr(s->buf.sink_k, s, step);
+  const char* bv = bank_ptr(s->buf.sink_v, s, step);
+  const Segment moving[sr::kSegs] = {{bk, bv, s->cfg.n_sink}, {nullptr, nullptr, 0}, {nullptr, nullptr, 0},
+                                     {k_moving, v_moving, M}};
+  const Segment prefix[sr::kSegs] = {{bk, bv, s->cfg.n_sink}, {nullptr, nullptr, 0}, {nullptr, nullptr, 0},
+                                     {nullptr, nullptr, 0}};
+  int n = 0, full = 0;
+  if (st == SR_OK) st = encode_group(p->sess[n++], moving, row_elems, P, M);
+  if (st == SR_OK && P > 0) st = encode_group(p->sess[n++], prefix, row_elems, 0, P);
+  if (st == SR_OK) {
+    for (int i = 0; i < n; ++i) {
+      p->sess[i].unit_begin = full;
+      p->sess[i].tail_begin = i * s->cfg.n_heads;
+      full += s->cfg.n_heads * (p->sess[i].nqb - 1);
+    }
+    p->n_full_units = full;
+    p->tail_split = 1;   // the groups share one session: no key-split workspace
+    p->n_sess = n;
+    p->n_heads = s->cfg.n_heads;
+    p->scale_log2 = s->scale * 1.4426950408889634f;
+    p->lse_ld = lse ? static_cast<int32_t>(P + M) : 0;
+    p->o = static_cast<__nv_bfloat16*>(o);
+    p->lse = lse;
+    p->err_word = s->buf.err_word;
+    p->timeout_ns = s->cfg.wait_timeout_ns;
+    cudaError_t e = sr::launch_attention_n(*p, s->cfg.head_dim, full + n * s->cfg.n_heads,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) st = SR_ERR_CUDA;
+  }
+  delete p;
+  return st;
 }
 
 sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32_t step, const void* q,

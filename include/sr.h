@@ -253,6 +253,35 @@ SR_API sr_status sr_chunk_attention_frames(sr_session* s, int32_t step, int32_t 
 SR_API sr_status sr_cache_commit_frames(sr_session* s, int32_t n_frames, const void* k_raw, const void* v,
                                         void* stream);
 
+/*
+ * The page-faithful window ([teardown] "A window that slides, and a prefix that
+ * doesn't"; [H3 page] 3.1.2 "Prefix cache"). The pages split each window into a
+ * fixed prefix (conditioning and sink, whose keys and values are the per-step bank)
+ * and a moving part (recent history and the chunk, recomputed every chunk), with an
+ * asymmetric mask: prefix rows attend only to the prefix, moving rows attend to the
+ * whole window. One launch computes both groups; the mask is expressed as each
+ * group's key set, so no score is masked:
+ *   prefix rows:  softmax(scale Q_p K_bank^T) V_bank
+ *   moving rows:  softmax(scale Q_m [K_bank; K_m]^T) [V_bank; V_m]
+ * moving_frames: latent frames of moving rows (history + chunk), M = moving_frames*T.
+ * q, o: [P + M][H][d] bf16 with P = n_sink when with_prefix != 0 (the prefix rows
+ * first, as the prefix pass of a session's first window), else P = 0.
+ * k_moving, v_moving: [M][H][d] bf16, the moving rows' keys and values (not the
+ * ring: this is the computation the ring path caches). lse: optional [H][P + M].
+ * with_prefix needs n_sink > 0. The ring and the frame count are not touched.
+ */
+SR_API sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames, int32_t with_prefix,
+                                     const void* q, const void* k_moving, const void* v_moving, void* o,
+                                     float* lse, void* stream);
+
+/*
+ * sr_rope3d_qk for rows of n_frames frames starting at the stream's frame
+ * first_frame (time t_clock0 + first_frame + f): recomputed history rows keep their
+ * own frame times. |first_frame| <= 2^40.
+ */
+SR_API sr_status sr_rope3d_qk_at(sr_session* s, int64_t first_frame, int32_t n_frames, void* q, void* k,
+                                 void* stream);
+
 /* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
 SR_API sr_status sr_device_error_status(int32_t err_word_value);
 
