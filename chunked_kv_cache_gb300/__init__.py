@@ -15,7 +15,8 @@ from ._native import (SrConfig, SrBuffers, SrError, sr_session_init, sr_session_
                       sr_rope3d_qk, sr_chunk_attention, sr_cache_commit, sr_session_free,
                       sr_chunk_attention_batch, sr_device_error_status, sr_debug_wait_timeout,
                       sr_workspace_bytes, sr_plan_chunk, sr_rope3d_qk_frames, sr_chunk_attention_frames,
-                      sr_cache_commit_frames, SrChunkPlan, sr_window_attention, sr_rope3d_qk_at, SR_MAX_BATCH)
+                      sr_cache_commit_frames, SrChunkPlan, sr_window_attention, sr_rope3d_qk_at,
+                      sr_rope3d_qk_dev, sr_chunk_attention_dev, sr_cache_commit_dev, SR_MAX_BATCH)
 
 __all__ = [
     "Session", "chunk_attention_batch", "SrConfig", "SrBuffers", "SrError",
@@ -23,7 +24,8 @@ __all__ = [
     "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch", "sr_device_error_status",
     "sr_debug_wait_timeout", "sr_workspace_bytes", "sr_plan_chunk", "sr_rope3d_qk_frames",
     "sr_chunk_attention_frames", "sr_cache_commit_frames", "SrChunkPlan", "plan_chunk",
-    "sr_window_attention", "sr_rope3d_qk_at",
+    "sr_window_attention", "sr_rope3d_qk_at", "sr_rope3d_qk_dev", "sr_chunk_attention_dev",
+    "sr_cache_commit_dev",
 ]
 
 _BF16 = torch.bfloat16
@@ -57,7 +59,7 @@ class Session:
                  window_frames: int, n_sink: int, n_steps: int = 2, *, sink_k: torch.Tensor | None = None,
                  sink_v: torch.Tensor | None = None, t_clock0: int = 0, rope_base: float = 10000.0,
                  softmax_scale: float = 0.0, wait_timeout_ns: int = 0, tail_split: int = 0,
-                 workspace: bool = True, device="cuda"):
+                 workspace: bool = True, device_state: bool = False, device="cuda"):
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
@@ -84,8 +86,11 @@ class Session:
         if workspace:
             nbytes = sr_workspace_bytes(self.cfg)
             self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        # device-resident frame counter for the *_dev calls (CUDA-graph capture)
+        self.frame_counter = torch.zeros((1,), dtype=torch.int64, device=dev) if device_state else None
         self.bufs = SrBuffers(_ptr(self.sink_k), _ptr(self.sink_v), _ptr(self.ring_k), _ptr(self.ring_v),
-                              self.slot_frame.data_ptr(), self.err_word.data_ptr(), _ptr(self.workspace))
+                              self.slot_frame.data_ptr(), self.err_word.data_ptr(), _ptr(self.workspace),
+                              _ptr(self.frame_counter))
         self.handle = None
         with torch.cuda.device(dev):
             self.handle = sr_session_init(self.cfg, self.bufs, _ptr(sink_k), _ptr(sink_v), _stream(dev))
@@ -150,6 +155,34 @@ class Session:
             sr_cache_commit(self.handle, k.data_ptr(), v.data_ptr(), _stream(self.device))
         else:
             sr_cache_commit_frames(self.handle, frames, k.data_ptr(), v.data_ptr(), _stream(self.device))
+
+    # ------------------------------------------------ device-resident chunk state
+    # The *_dev calls read the committed-frame count from self.frame_counter when
+    # the kernels run (Session(device_state=True)); a captured sequence of them
+    # serves every chunk of its length.
+    def rope3d_qk_dev(self, q: torch.Tensor | None, k: torch.Tensor | None, frames: int) -> None:
+        for name, t in (("q", q), ("k", k)):
+            if t is not None:
+                self._chunk(name, t, frames)
+        sr_rope3d_qk_dev(self.handle, frames, _ptr(q), _ptr(k), _stream(self.device))
+
+    def chunk_attention_dev(self, step: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, frames: int,
+                            hist: int = -1, out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            self._chunk(name, t, frames)
+        if out is None:
+            out = torch.empty_like(q)
+        self._chunk("out", out, frames)
+        if lse is not None:
+            _check_tensor("lse", lse, (self.H, q.shape[0]), self.device, torch.float32)
+        sr_chunk_attention_dev(self.handle, step, frames, hist, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               out.data_ptr(), _ptr(lse), _stream(self.device))
+        return out
+
+    def cache_commit_dev(self, k: torch.Tensor, v: torch.Tensor, frames: int) -> None:
+        self._chunk("k", k, frames)
+        self._chunk("v", v, frames)
+        sr_cache_commit_dev(self.handle, frames, k.data_ptr(), v.data_ptr(), _stream(self.device))
 
     # ------------------------------------------------ the page-faithful window
     def rope3d_at(self, first_frame: int, frames: int, q: torch.Tensor | None, k: torch.Tensor | None) -> None:

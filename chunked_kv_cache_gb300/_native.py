@@ -28,7 +28,8 @@ EXPORTS = (
     "sr_chunk_attention", "sr_cache_commit", "sr_session_free", "sr_chunk_attention_batch",
     "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string", "sr_workspace_bytes",
     "sr_chunk_attention_noalloc", "sr_plan_chunk", "sr_rope3d_qk_frames", "sr_chunk_attention_frames",
-    "sr_cache_commit_frames", "sr_window_attention", "sr_rope3d_qk_at",
+    "sr_cache_commit_frames", "sr_window_attention", "sr_rope3d_qk_at", "sr_rope3d_qk_dev",
+    "sr_chunk_attention_dev", "sr_cache_commit_dev",
 )
 
 
@@ -49,7 +50,7 @@ class SrBuffers(ctypes.Structure):
         ("sink_k", ctypes.c_void_p), ("sink_v", ctypes.c_void_p),
         ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p),
         ("slot_frame", ctypes.c_void_p), ("err_word", ctypes.c_void_p),
-        ("workspace", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("frame_counter", ctypes.c_void_p),
     ]
 
 
@@ -93,6 +94,9 @@ def lib() -> ctypes.CDLL:
         L.sr_cache_commit_frames.argtypes = [vp, i32, vp, vp, vp]
         L.sr_window_attention.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.sr_rope3d_qk_at.argtypes = [vp, i64, i32, vp, vp, vp]
+        L.sr_rope3d_qk_dev.argtypes = [vp, i32, vp, vp, vp]
+        L.sr_chunk_attention_dev.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.sr_cache_commit_dev.argtypes = [vp, i32, vp, vp, vp]
         L.sr_chunk_attention_batch.argtypes = [ctypes.POINTER(vp), i32, i32, vp, vp, vp,
                                                ctypes.POINTER(i64), vp, vp, vp]
         L.sr_device_error_status.argtypes = [i32]
@@ -181,6 +185,20 @@ def sr_window_attention(handle: int, step: int, moving_frames: int, with_prefix:
 def sr_rope3d_qk_at(handle: int, first_frame: int, n_frames: int, q: int, k: int, stream: int) -> None:
     _check(lib().sr_rope3d_qk_at(handle, int(first_frame), int(n_frames), q or None, k or None, stream or None),
            "sr_rope3d_qk_at")
+
+
+def sr_rope3d_qk_dev(handle: int, n_frames: int, q: int, k: int, stream: int) -> None:
+    _check(lib().sr_rope3d_qk_dev(handle, int(n_frames), q or None, k or None, stream or None), "sr_rope3d_qk_dev")
+
+
+def sr_chunk_attention_dev(handle: int, step: int, n_frames: int, hist_frames: int, q: int, k: int, v: int, o: int,
+                           lse: int, stream: int) -> None:
+    _check(lib().sr_chunk_attention_dev(handle, int(step), int(n_frames), int(hist_frames), q, k, v, o, lse or None,
+                                        stream or None), "sr_chunk_attention_dev")
+
+
+def sr_cache_commit_dev(handle: int, n_frames: int, k_raw: int, v: int, stream: int) -> None:
+    _check(lib().sr_cache_commit_dev(handle, int(n_frames), k_raw, v, stream or None), "sr_cache_commit_dev")
 
 
 def sr_chunk_attention_noalloc(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int,

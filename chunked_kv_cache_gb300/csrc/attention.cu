@@ -79,6 +79,22 @@ struct Cfg {
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 1);
 };
 
+// Key tiles of a unit: segment s has nt[s] tiles over rows[s] valid rows,
+// which start at row base[s] of its tensor map.
+struct TileMap {
+  int nt[kSegs];
+  int rows[kSegs];
+  int base[kSegs];
+  __device__ __forceinline__ void locate(int j, int& seg, int& row0) const {
+    seg = 0;
+    while (seg < kSegs - 1 && j >= nt[seg]) {
+      j -= nt[seg];
+      ++seg;
+    }
+    row0 = j * BN;
+  }
+};
+
 struct SmemBars {
   uint64_t q_full;
   uint64_t kv_full[8];    // up to kStagesSplit stages
@@ -92,18 +108,7 @@ struct SmemBars {
   int last;       // key-split last block: this CTA is the last part and merges
   float xm[BM];   // split mode: group 1's running max / sum, handed to group 0
   float xl[BM];
-};
-
-struct TileMap {
-  int nt[kSegs];
-  __device__ __forceinline__ void locate(int j, int& seg, int& row0) const {
-    seg = 0;
-    while (seg < kSegs - 1 && j >= nt[seg]) {
-      j -= nt[seg];
-      ++seg;
-    }
-    row0 = j * BN;
-  }
+  TileMap tm;     // the unit's key tiles, read by the producer and the softmax groups
 };
 
 // The key tiles each query tile walks, within the unit's range [lo, lo + n) of
@@ -161,13 +166,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const AttnSession& S = p.sess[si];
   const int q_local0 = qb * 2 * BM;                       // first query row of the unit (session-local)
   const int n_qtiles = min(2, (S.lq - q_local0 + BM - 1) / BM);
-  TileMap tm;
+  TileMap tl;   // registers only here; the loops read the shared-memory copy
 #pragma unroll
+  for (int s = 0; s < kSegs; ++s) {
+    tl.rows[s] = S.seg_rows[s];
+    tl.base[s] = 0;
+  }
+  if (S.dev_n != nullptr) {
+    // The visible ring frames follow the device frame counter: frames n-h ..
+    // n-1 in slots (g mod W), one or two row ranges of the whole-ring maps.
+    const int64_t n = *S.dev_n;
+    const int W = S.ring_W, T = S.ring_T;
+    const int v = static_cast<int>(min(n, static_cast<int64_t>(W)));
+    const int h = S.hist_req < 0 ? v : min(S.hist_req, v);
+    if (h == W) {
+      tl.rows[1] = W * T;
+      tl.rows[2] = 0;
+    } else if (h > 0) {
+      const int start = static_cast<int>((n - h) % W);
+      const int a = min(h, W - start);
+      tl.base[1] = start * T;
+      tl.rows[1] = a * T;
+      tl.rows[2] = (h - a) * T;
+    } else {
+      tl.rows[1] = tl.rows[2] = 0;
+    }
+  }
   int n_kv_all = 0;
 #pragma unroll
   for (int s = 0; s < kSegs; ++s) {
-    tm.nt[s] = (S.seg_rows[s] + BN - 1) / BN;
-    n_kv_all += tm.nt[s];
+    tl.nt[s] = (tl.rows[s] + BN - 1) / BN;
+    n_kv_all += tl.nt[s];
   }
   // a single-tile last block may be one of `parts` CTAs sharing its key range
   const int parts = (n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
@@ -178,6 +207,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   WaitCtx wc{&bars->abort, p.err_word, p.timeout_ns};
 
   if (threadIdx.x == 0) {
+    bars->tm = tl;
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < C::kStagesSplit; ++s) {
       mbar_init(&bars->kv_full[s], 1);
@@ -200,6 +230,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  const TileMap& tm = bars->tm;
 
   if (warp >= 8) {
     regs_dec<kRegsOther>();
@@ -234,7 +265,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         mbar_arrive_expect_tx(&bars->kv_full[stage], C::kTileBytes);
         uint8_t* dst = stage < C::kStages ? sKV + stage * C::kTileBytes : sQ + C::kTileBytes;
         for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_2d(dst + a * C::kAtomBytes, map, &bars->kv_full[stage], head * D + a * 64, row0, pol_kv);
+          tma_load_2d(dst + a * C::kAtomBytes, map, &bars->kv_full[stage], head * D + a * 64, tm.base[seg] + row0,
+                      pol_kv);
         ++idx;
       };
       const int n_it = wk.iters();
@@ -434,6 +466,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     const int cnt = wk.count(t);
     bool ok = true;
     for (int j = 0; ok && j < cnt; ++j) {
+      // ragged tail of a segment: keys past its end are not part of the window.
+      // Looked up before the wait, so the shared-memory latency hides behind it.
+      int seg, row0;
+      tm.locate(wk.kv(t, j), seg, row0);
+      const int valid = tm.rows[seg] - row0;
       ok = wait_bounded(&bars->s_full[t], j & 1, wc, 5);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -445,10 +482,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_fix(r[c]);
       float* s = reinterpret_cast<float*>(&r[0][0]);
-      // ragged tail of a segment: keys past its end are not part of the window
-      int seg, row0;
-      tm.locate(wk.kv(t, j), seg, row0);
-      const int valid = S.seg_rows[seg] - row0;
       if (valid < BN) {
 #pragma unroll
         for (int i = 0; i < BN; ++i)

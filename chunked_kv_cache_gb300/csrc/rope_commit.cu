@@ -51,11 +51,13 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, 
   if (tok_lo >= p.n_tok) return;
   const int ntok = min(tokens_per_cta, p.n_tok - tok_lo);
   const int nvec = ntok * vpt;
+  // frames committed before this chunk: from the device counter when one is given
+  const int64_t n0 = (p.dev_n != nullptr ? *p.dev_n : 0) + p.n_committed;
 
   // Slot table: frame g = n + f now lives in slot g mod W.
   if (p.mode == 1 && blockIdx.x == 0) {
     for (int f = threadIdx.x; f < p.chunk_frames; f += kRopeThreads) {
-      const int64_t g = p.n_committed + f;
+      const int64_t g = n0 + f;
       p.slot_frame[g % p.window_frames] = static_cast<int32_t>(g);
     }
   }
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, 
         const int in_frame = tok % p.tokens_per_frame;
         int64_t pos;
         if (ax == 0)
-          pos = p.t_clock0 + p.n_committed + tok / p.tokens_per_frame;
+          pos = p.t_clock0 + n0 + tok / p.tokens_per_frame;
         else if (ax == 1)
           pos = in_frame / p.grid_w;
         else
@@ -117,7 +119,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, 
         } else {
           const int f = tok / p.tokens_per_frame;
           const int r = tok - f * p.tokens_per_frame;
-          const int slot = static_cast<int>((p.n_committed + f) % p.window_frames);
+          const int slot = static_cast<int>((n0 + f) % p.window_frames);
           dst_row[t] = slot * p.tokens_per_frame + r;
         }
       }
@@ -196,6 +198,15 @@ __global__ void init_ring_state_kernel(int32_t* slot_frame, int W, int32_t* err_
   if (threadIdx.x == 0) *err_word = SR_DEVERR_NONE;
 }
 }  // namespace
+
+// Advance the device frame counter after a commit: its own launch, so that
+// every CTA of the commit read the old value.
+__global__ void advance_frames_kernel(int64_t* counter, int64_t add) { *counter += add; }
+
+cudaError_t launch_advance_frames(int64_t* counter, int64_t add, cudaStream_t st) {
+  advance_frames_kernel<<<1, 1, 0, st>>>(counter, add);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(bytes / 16);

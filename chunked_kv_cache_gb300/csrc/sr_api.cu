@@ -142,8 +142,10 @@ cudaError_t ensure_attn_attr(int head_dim, int nsess_template) {
 // What one attention call of a session sees: the chunk's query/key rows and
 // how many of the most recent committed frames are visible.
 struct ChunkView {
-  int64_t lq;     // chunk rows, frames * T
-  int64_t hist;   // visible history: the last `hist` committed frames
+  int64_t lq;         // chunk rows, frames * T
+  int64_t hist;       // visible history: the last `hist` committed frames (host-state calls)
+  bool dev = false;   // device-state call: the kernel derives the history from the frame counter
+  int32_t hist_req = -1;   // ... of this many frames (-1: every occupied slot)
 };
 
 // The plain calls: the configured chunk length and every occupied slot.
@@ -209,7 +211,12 @@ sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& vie
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
   const size_t row_bytes = static_cast<size_t>(row_elems) * 2;
   int64_t r0 = 0, c0 = 0, c1 = 0;
-  ring_ranges(s, view.hist, r0, c0, c1);
+  if (view.dev) {
+    // both ring segments map the whole ring; the kernel picks the rows
+    c0 = c1 = s->cfg.window_frames * s->tokens_per_frame;
+  } else {
+    ring_ranges(s, view.hist, r0, c0, c1);
+  }
   const size_t ring_off = static_cast<size_t>(r0) * row_bytes;
   const Segment seg[sr::kSegs] = {
       {bank_ptr(s->buf.sink_k, s, step), bank_ptr(s->buf.sink_v, s, step), s->cfg.n_sink},
@@ -219,6 +226,12 @@ sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& vie
        static_cast<const char*>(v) + static_cast<size_t>(row0) * row_bytes, view.lq}};
   sr_status st = encode_group(out, seg, row_elems, row0, view.lq);
   if (st != SR_OK) return st;
+  if (view.dev) {
+    out.dev_n = s->buf.frame_counter;
+    out.hist_req = view.hist_req;
+    out.ring_W = s->cfg.window_frames;
+    out.ring_T = static_cast<int32_t>(s->tokens_per_frame);
+  }
   if (s->buf.workspace) {
     char* ws = static_cast<char*>(s->buf.workspace);
     out.ws_ctr = reinterpret_cast<int32_t*>(ws);
@@ -233,7 +246,8 @@ sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& vie
 // Key tiles a session's chunk attends over (sink bank + visible ring + chunk).
 int64_t key_tiles(const sr_session* s, const ChunkView& view) {
   int64_t r0 = 0, c0 = 0, c1 = 0;
-  ring_ranges(s, view.hist, r0, c0, c1);
+  // a device-state call may see anything from no ring frame up: plan for none
+  if (!view.dev) ring_ranges(s, view.hist, r0, c0, c1);
   const int64_t rows[4] = {s->cfg.n_sink, c0, c1, view.lq};
   int64_t n = 0;
   for (int64_t r : rows) n += (r + 127) / 128;
@@ -361,7 +375,8 @@ sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const vo
       (sink_k_src && (!aligned16(sink_k_src) || !aligned16(sink_v_src))) ||
       (reinterpret_cast<uintptr_t>(bufs->err_word) & 3u) ||
       (reinterpret_cast<uintptr_t>(bufs->workspace) & 255u) ||
-      (reinterpret_cast<uintptr_t>(bufs->slot_frame) & 3u))
+      (reinterpret_cast<uintptr_t>(bufs->slot_frame) & 3u) ||
+      (reinterpret_cast<uintptr_t>(bufs->frame_counter) & 7u))
     return SR_ERR_ALIGN;
 
   sr_session* s = new (std::nothrow) sr_session;
@@ -386,6 +401,15 @@ sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const vo
   if (e == cudaSuccess)
     e = sr::launch_init_ring_state(bufs->slot_frame, cfg->window_frames, bufs->err_word,
                                    static_cast<int32_t*>(bufs->workspace), cfg->n_heads, cs);
+  if (e == cudaSuccess && bufs->frame_counter) {
+    // device-state calls: the counter starts at 0, and ring tiles that straddle
+    // the visible rows read zeros rather than whatever the buffers held
+    e = cudaMemsetAsync(bufs->frame_counter, 0, sizeof(int64_t), cs);
+    const size_t ring_bytes = static_cast<size_t>(cfg->window_frames) * s->tokens_per_frame * cfg->n_heads *
+                              cfg->head_dim * 2;
+    if (e == cudaSuccess && ring_bytes) e = cudaMemsetAsync(bufs->ring_k, 0, ring_bytes, cs);
+    if (e == cudaSuccess && ring_bytes) e = cudaMemsetAsync(bufs->ring_v, 0, ring_bytes, cs);
+  }
   if (e == cudaSuccess) e = ensure_attn_attr(cfg->head_dim, 1);
   if (e == cudaSuccess) e = ensure_attn_attr(cfg->head_dim, sr::kAttnMaxBatch);
   if (e != cudaSuccess) {
@@ -422,7 +446,8 @@ static bool frames_ok(const sr_session* s, int64_t n_frames) {
 // stream's frame first_frame + f, with time t_clock0 + first_frame + f (the
 // chunk calls pass n_committed).
 static sr_status rope_common(sr_session* s, int64_t first_frame, int64_t n_frames, const void* a_src,
-                             const void* b_src, void* a_dst, void* b_dst, int mode, void* stream) {
+                             const void* b_src, void* a_dst, void* b_dst, int mode, void* stream,
+                             const int64_t* dev_n = nullptr) {
   sr::RopeParams p;
   std::memset(&p, 0, sizeof(p));
   int64_t first = 0;   // first frame of the chunk that is processed
@@ -447,6 +472,7 @@ static sr_status rope_common(sr_session* s, int64_t first_frame, int64_t n_frame
     p.inv_freq_lo[i] = static_cast<float>(s->inv_freq[i] - static_cast<double>(p.inv_freq_hi[i]));
   }
   std::memcpy(p.axis, s->axis, sizeof(p.axis));
+  p.dev_n = dev_n;   // when set, first_frame is an offset from the device counter
   cudaError_t e = sr::launch_rope(p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SR_OK : SR_ERR_CUDA;
 }
@@ -548,6 +574,41 @@ sr_status sr_chunk_attention_frames(sr_session* s, int32_t step, int32_t n_frame
   if (hist_frames < -1 || hist_frames > occupied) return SR_ERR_INVALID_ARG;
   const ChunkView view{n_frames * s->tokens_per_frame, hist_frames == -1 ? occupied : hist_frames};
   return attention_view(s, view, step, q, k, v, o, lse, stream);
+}
+
+sr_status sr_rope3d_qk_dev(sr_session* s, int32_t n_frames, void* q, void* k, void* stream) {
+  if (!s || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
+  if (!s->buf.frame_counter) return SR_ERR_STATE;
+  if ((q && !aligned16(q)) || (k && !aligned16(k))) return SR_ERR_ALIGN;
+  if (!q && !k) return SR_OK;
+  if (q && k) return rope_common(s, 0, n_frames, q, k, q, k, 0, stream, s->buf.frame_counter);
+  void* x = q ? q : k;
+  return rope_common(s, 0, n_frames, x, x, x, x, 0, stream, s->buf.frame_counter);
+}
+
+sr_status sr_chunk_attention_dev(sr_session* s, int32_t step, int32_t n_frames, int32_t hist_frames,
+                                 const void* q, const void* k, const void* v, void* o, float* lse, void* stream) {
+  if (!s || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
+  if (!s->buf.frame_counter) return SR_ERR_STATE;
+  if (hist_frames < -1 || hist_frames > s->cfg.window_frames) return SR_ERR_INVALID_ARG;
+  ChunkView view{n_frames * s->tokens_per_frame, 0};
+  view.dev = true;
+  view.hist_req = hist_frames;
+  return attention_view(s, view, step, q, k, v, o, lse, stream);
+}
+
+sr_status sr_cache_commit_dev(sr_session* s, int32_t n_frames, const void* k_raw, const void* v, void* stream) {
+  if (!s || !k_raw || !v || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
+  if (!s->buf.frame_counter) return SR_ERR_STATE;
+  if (!aligned16(k_raw) || !aligned16(v)) return SR_ERR_ALIGN;
+  sr_status st = SR_OK;
+  if (s->cfg.window_frames > 0)   // frame times and slots from the device counter (offset 0)
+    st = rope_common(s, 0, n_frames, k_raw, v, s->buf.ring_k, s->buf.ring_v, 1, stream, s->buf.frame_counter);
+  if (st == SR_OK &&
+      sr::launch_advance_frames(s->buf.frame_counter, n_frames, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    st = SR_ERR_CUDA;
+  if (st == SR_OK) s->n_committed += n_frames;   // the host mirror follows eager calls, not graph replays
+  return st;
 }
 
 sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames, int32_t with_prefix,

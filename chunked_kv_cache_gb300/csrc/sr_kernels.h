@@ -31,6 +31,13 @@ struct alignas(128) AttnSession {
   float* ws_part;       // key-split partials: [H][kMaxTailSplit][128][d + 4] fp32 (NULL: no split)
   int32_t* ws_ctr;      // [H] per-head arrival counters (epoch << 4 | count)
   int32_t epoch;        // this call's epoch for the counters (increases per call of the session)
+  // Device frame counter (NULL: the host filled seg_rows). When set, segments 1
+  // and 2 are maps over the whole ring and the kernel derives the visible ring
+  // rows from *dev_n: the last hist_req committed frames (-1: every occupied slot).
+  const int64_t* dev_n;
+  int32_t hist_req;
+  int32_t ring_W;
+  int32_t ring_T;
 };
 
 template <int NSESS>
@@ -77,6 +84,8 @@ struct RopeParams {
   int32_t t_clock0;
   int32_t mode;                // 0: rotate src0->dst0 and src1->dst1 in place; 1: commit
   int8_t axis[64];             // 0 = t, 1 = h, 2 = w
+  const int64_t* dev_n;        // device frame counter: when set, frame f's time and slot use
+                               // *dev_n + n_committed + f (n_committed is then an offset)
 };
 
 cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st);
@@ -85,6 +94,7 @@ cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st);
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);
 cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, int32_t* ws_ctr, int n_ctr,
                                    cudaStream_t st);
+cudaError_t launch_advance_frames(int64_t* counter, int64_t add, cudaStream_t st);
 
 constexpr int kMaxTailSplit = SR_MAX_TAIL_SPLIT;
 

@@ -95,6 +95,9 @@ typedef struct {
   void* workspace;          /* optional, 256-byte aligned, sr_workspace_bytes() long: partial
                                results of key-split last blocks. NULL disables the split. The
                                library initialises it in sr_session_init; do not modify it after. */
+  int64_t* frame_counter;   /* optional [1] int64 device: the committed-frame count the *_dev calls
+                               read and advance on the device (NULL: those calls are refused).
+                               When given, sr_session_init zeroes it and zero-fills ring_k/ring_v. */
 } sr_buffers;
 
 #define SR_MAX_TAIL_SPLIT 4
@@ -281,6 +284,32 @@ SR_API sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving
  */
 SR_API sr_status sr_rope3d_qk_at(sr_session* s, int64_t first_frame, int32_t n_frames, void* q, void* k,
                                  void* stream);
+
+/*
+ * Device-resident chunk state, for CUDA-graph capture of the per-chunk sequence
+ * ([H3 page] 3.3 "Attention metadata reuse": the per-call metadata is prepared once
+ * and no call waits on the host). These calls compute exactly what sr_rope3d_qk_frames,
+ * sr_chunk_attention_frames and sr_cache_commit_frames compute, but the
+ * committed-frame count n is read from bufs->frame_counter when the kernels run, and
+ * sr_cache_commit_dev advances it on the device (one more tiny launch). One captured
+ * sequence of these calls therefore serves every chunk of its length:
+ *   capture:  rope_dev(step 0), attention_dev(0), rope_dev(1), attention_dev(1), commit_dev
+ *   replay:   once per chunk, after copying the chunk's inputs into the captured buffers.
+ * The visible ring rows come from the counter (hist_frames as in
+ * sr_chunk_attention_frames, -1 = every occupied slot, otherwise at most W; fewer
+ * frames are seen while fewer are committed). Ring tiles that straddle the end of the
+ * visible rows read neighbouring ring rows with zero weight, so the ring must hold
+ * finite values: sr_session_init zero-fills it when a frame_counter is given.
+ * The host mirror of n (sr_session_frames) does not follow replays; sr_session_restore
+ * re-synchronises it before host-state calls are mixed in.
+ * Without a frame_counter: SR_ERR_STATE.
+ */
+SR_API sr_status sr_rope3d_qk_dev(sr_session* s, int32_t n_frames, void* q, void* k, void* stream);
+SR_API sr_status sr_chunk_attention_dev(sr_session* s, int32_t step, int32_t n_frames, int32_t hist_frames,
+                                        const void* q, const void* k, const void* v, void* o, float* lse,
+                                        void* stream);
+SR_API sr_status sr_cache_commit_dev(sr_session* s, int32_t n_frames, const void* k_raw, const void* v,
+                                     void* stream);
 
 /* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
 SR_API sr_status sr_device_error_status(int32_t err_word_value);
