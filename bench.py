@@ -9,12 +9,12 @@ used alternately, so every step reads inputs that were last touched more
 than an L2's worth of traffic ago.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2|3]
-                    [--workload steady|rhythm|window]
+                    [--workload steady|rhythm|window|graph]
 
 ``--workload rhythm`` times the pages' unit rhythm instead (chunks of 3 and 2
 latent frames at the 832x480 frame size) and ``--workload window`` the
-page-faithful window (recomputed history rows as queries); each prints its own
-line.
+page-faithful window (recomputed history rows as queries), ``--workload graph``
+a chunk issued eagerly against one CUDA-graph replay; each prints its own line.
 
 Multi-GPU: the path has no exchange step, so N ranks run N independent
 replicas (weak scaling, no collective on the data path); rank 0 prints the
@@ -611,6 +611,77 @@ def run_window(args):
     print(json.dumps(out), flush=True)
 
 
+def run_graph(args):
+    """Per-chunk sequence (2 x (RoPE + attention) + commit) issued eagerly
+    through the device-state calls, against one CUDA-graph replay of the same
+    sequence, in steady state (ring full). Two shapes: the 832x480 chunk, and a
+    small one (4 heads x 64, 6x10 tokens per frame, 64 sink rows, W = 4) where
+    launch and host overhead dominate. Reports device ms per chunk (CUDA events
+    around K chunks) and host microseconds to issue one chunk."""
+    import chunked_kv_cache_gb300 as sr
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_kv_cache_gb300 import build
+    build.build()
+    shapes = {"832x480": syn.SHAPES[2], "small 4x64 6x10 S=64 W=4": syn.SHAPES[1]}
+    results = {}
+    for name, sh in shapes.items():
+        T, H, d, F, W = sh.tokens_per_frame, sh.n_heads, sh.head_dim, sh.chunk_frames, sh.window_frames
+        sink = lambda tid: syn.device_normal_bf16((sh.n_steps, sh.n_sink, H, d), dev, 7, 0, 0, 0, tid)
+        s = sr.Session(H, d, sh.grid_h, sh.grid_w, F, W, sh.n_sink, sh.n_steps, sink_k=sink(syn.T_SINK_K),
+                       sink_v=sink(syn.T_SINK_V), device_state=True, device=dev)
+        x = syn.chunk_inputs_device(sh, 7, dev, chunk=1)
+        o = [torch.empty_like(x["q"][0]) for _ in range(sh.n_steps)]
+
+        def chunk():
+            for st in range(sh.n_steps):
+                s.rope3d_qk_dev(x["q"][st], x["k"][st], F)
+                s.chunk_attention_dev(st, x["q"][st], x["k"][st], x["v"][st], F, out=o[st])
+            s.cache_commit_dev(x["clean_k"], x["clean_v"], F)
+
+        for _ in range(W // F + max(args.warmup, 3)):      # fill the ring, then warm up
+            chunk()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chunk()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        res = {}
+        for mode, fn in (("eager", chunk), ("graph", g.replay)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            h0 = time.perf_counter()
+            for _ in range(args.steps):
+                fn()
+            host_us = (time.perf_counter() - h0) / args.steps * 1e6
+            b.record()
+            torch.cuda.synchronize()
+            res[mode] = {"ms_per_chunk": round(a.elapsed_time(b) / args.steps, 4), "host_us_per_chunk": round(host_us, 1)}
+        if s.error_status() != 0:
+            raise RuntimeError("device error word set during the bench")
+        res["speedup"] = round(res["eager"]["ms_per_chunk"] / res["graph"]["ms_per_chunk"], 3)
+        results[name] = res
+        s.close()
+    main = results["832x480"]
+    out = {
+        "metric": "per-chunk time, eager calls vs CUDA-graph replay (device-resident chunk state), 1 GB300",
+        "value": main["graph"]["ms_per_chunk"], "unit": "ms/chunk", "higher_is_better": False, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "steady state (ring full), one step = one chunk: 2 x (RoPE-3D + chunk attention) + "
+                               "ring commit through the *_dev calls; eager vs one graph replay"},
+        "shapes": results,
+        "gpu_launches": 6 * args.steps,
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,9 +689,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, choices=[2, 3], default=2)
-    ap.add_argument("--workload", choices=["steady", "rhythm", "window"], default="steady",
+    ap.add_argument("--workload", choices=["steady", "rhythm", "window", "graph"], default="steady",
                     help="steady: the headline chunk workload; rhythm: the pages' 3/2-latent unit rhythm; "
-                         "window: the page-faithful window (recomputed history rows as queries)")
+                         "window: the page-faithful window (recomputed history rows as queries); "
+                         "graph: eager calls vs CUDA-graph replay of a chunk")
     ap.add_argument("--profile", action="store_true",
                     help="under a profiler: skip the end-to-end and CPU-baseline legs (their numbers are not reported)")
     args = ap.parse_args()
@@ -632,6 +704,8 @@ def main():
         run_rhythm(args)
     elif args.workload == "window":
         run_window(args)
+    elif args.workload == "graph":
+        run_graph(args)
     else:
         run_ours(args)
 
