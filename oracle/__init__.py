@@ -26,6 +26,9 @@ What it computes, and where the pages define it. The pages are
   that doesn't"), two steps then commit; chunks of any number of frames and
   a recent history of the last h committed frames; the page-faithful window
   (prefix rows see only the prefix, recomputed moving rows see everything).
+* ``decoder``    the streaming decoder's window attention, one layer: windows
+  of 16x16 tokens, shifted every other layer, each seeing the global tokens,
+  its cached frames and its chunk ([H3-page] 3.2 Iterations 2-4).
 * ``schedule``   the scheduling units (2, 1, 1, 1 latents), the 7-unit first
   window and the per-chunk plan ([teardown] "A window that slides, and a
   prefix that doesn't"; [H3-page] 3.1.2).
