@@ -9,12 +9,13 @@ used alternately, so every step reads inputs that were last touched more
 than an L2's worth of traffic ago.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2|3]
-                    [--workload steady|rhythm|window|graph]
+                    [--workload steady|rhythm|window|graph|decoder]
 
 ``--workload rhythm`` times the pages' unit rhythm instead (chunks of 3 and 2
 latent frames at the 832x480 frame size) and ``--workload window`` the
 page-faithful window (recomputed history rows as queries), ``--workload graph``
-a chunk issued eagerly against one CUDA-graph replay; each prints its own line.
+a chunk issued eagerly against one CUDA-graph replay, ``--workload decoder``
+the streaming decoder's window attention per layer; each prints its own line.
 
 Multi-GPU: the path has no exchange step, so N ranks run N independent
 replicas (weak scaling, no collective on the data path); rank 0 prints the
@@ -682,6 +683,74 @@ def run_graph(args):
     print(json.dumps(out), flush=True)
 
 
+def run_decoder(args):
+    """The streaming decoder's window attention, one layer at a time, with a
+    full cache (4 frames) and 5 global tokens: every 16x16-token window's 2-frame
+    chunk (512 rows for a full window) over global tokens + its 4 cached frames +
+    its chunk (1541 keys for a full window). Latent grids of the 720p and the
+    pages' 768x1344 streams; 16 heads x 128 (a synthetic model shape: the pages
+    give no head count). Plain and shifted layers (the shifted one has partial
+    windows at the edges); attention only, inputs already packed per window."""
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_kv_cache_gb300 import build
+    build.build()
+    from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
+    H, d, G = 16, 128, 5
+    grids = {"720p (45x80 tokens)": (45, 80), "768x1344 (48x84 tokens)": (48, 84)}
+    results = {}
+    peak_tf, _, peak_kind = _peaks()
+    for gname, (gh, gw) in grids.items():
+        for shifted in (False, True):
+            lay = DecoderWindowLayer(gh, gw, H, d, G, shifted=shifted, device=dev)
+            rows = lay.rows
+            mk = lambda tid: syn.device_normal_bf16((rows, H, d), dev, 8, int(shifted), 0, 0, tid)
+            q, k, v = mk(syn.T_Q), mk(syn.T_K), mk(syn.T_V)
+            ck, cv = mk(syn.T_CLEAN_K), mk(syn.T_CLEAN_V)
+            lay.set_global(syn.device_normal_bf16((G, H, d), dev, 8, 0, 0, 0, syn.T_SINK_K),
+                           syn.device_normal_bf16((G, H, d), dev, 8, 0, 0, 0, syn.T_SINK_V))
+            for _ in range(2):                     # fill the 4-frame caches
+                lay.commit(ck, cv)
+            o = torch.empty_like(q)
+            for _ in range(max(args.warmup, 3)):
+                lay.attention(q, k, v, out=o)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(args.steps):
+                lay.attention(q, k, v, out=o)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / args.steps
+            fl = sum(4.0 * H * s.lq * (G + 6 * s.T) * d for s in lay.sessions)
+            full = [s for s in lay.sessions if s.T == 256]
+            results[f"{gname}, {'shifted' if shifted else 'plain'} layer"] = {
+                "windows": len(lay.windows), "full_windows": len(full), "launches": len(lay.groups),
+                "ms_per_layer": round(ms, 4), "tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+            if lay.error_status() != 0:
+                raise RuntimeError("device error word set during the bench")
+            lay.close()
+    key = "768x1344 (48x84 tokens), shifted layer"
+    out = {
+        "metric": "decoder window attention ms per layer on 1 GB300", "value": results[key]["ms_per_layer"],
+        "unit": "ms/layer", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "streaming decoder layer: 16x16-token windows, 2-frame chunk, 4 cached frames, "
+                               "5 global tokens, 16 heads x 128 (synthetic); windows batched per launch "
+                               "(at most 16); full cache; attention only"},
+        "layers": results,
+        "context": "pages: FlexAttention with a block mask, 6 ms per layer on GB200 (their 1.62B decoder)",
+        "roofline": {"bound": "tensor", "achieved": results[key]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(results[key]["tflops"] / peak_tf, 4),
+                     "kernel": "attn_kernel<128,16> (sr_chunk_attention_batch)", "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "gpu_launches": sum(v["launches"] for v in results.values()) * args.steps,
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -689,10 +758,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, choices=[2, 3], default=2)
-    ap.add_argument("--workload", choices=["steady", "rhythm", "window", "graph"], default="steady",
+    ap.add_argument("--workload", choices=["steady", "rhythm", "window", "graph", "decoder"], default="steady",
                     help="steady: the headline chunk workload; rhythm: the pages' 3/2-latent unit rhythm; "
                          "window: the page-faithful window (recomputed history rows as queries); "
-                         "graph: eager calls vs CUDA-graph replay of a chunk")
+                         "graph: eager calls vs CUDA-graph replay of a chunk; decoder: the streaming decoder's "
+                         "window attention")
     ap.add_argument("--profile", action="store_true",
                     help="under a profiler: skip the end-to-end and CPU-baseline legs (their numbers are not reported)")
     args = ap.parse_args()
@@ -706,6 +776,8 @@ def main():
         run_window(args)
     elif args.workload == "graph":
         run_graph(args)
+    elif args.workload == "decoder":
+        run_decoder(args)
     else:
         run_ours(args)
 

@@ -59,7 +59,7 @@ class Session:
                  window_frames: int, n_sink: int, n_steps: int = 2, *, sink_k: torch.Tensor | None = None,
                  sink_v: torch.Tensor | None = None, t_clock0: int = 0, rope_base: float = 10000.0,
                  softmax_scale: float = 0.0, wait_timeout_ns: int = 0, tail_split: int = 0,
-                 workspace: bool = True, device_state: bool = False, device="cuda"):
+                 workspace: bool = True, device_state: bool = False, bank=None, device="cuda"):
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
@@ -68,8 +68,17 @@ class Session:
         self.F, self.W, self.S, self.n_steps = chunk_frames, window_frames, n_sink, n_steps
         self.lq = chunk_frames * self.T
         dev = self.device
-        self.sink_k = torch.empty((n_steps, n_sink, n_heads, head_dim), dtype=_BF16, device=dev)
-        self.sink_v = torch.empty_like(self.sink_k)
+        if bank is not None:
+            # an external bank, possibly shared by several sessions (the decoder's
+            # windows share the global tokens); used in place, not copied
+            if sink_k is not None or sink_v is not None:
+                raise ValueError("give bank or sink_k/sink_v, not both")
+            self.sink_k, self.sink_v = bank
+            for name, t in (("bank k", self.sink_k), ("bank v", self.sink_v)):
+                _check_tensor(name, t, (n_steps, n_sink, n_heads, head_dim), dev)
+        else:
+            self.sink_k = torch.empty((n_steps, n_sink, n_heads, head_dim), dtype=_BF16, device=dev)
+            self.sink_v = torch.empty_like(self.sink_k)
         self.ring_k = torch.empty((window_frames * self.T, n_heads, head_dim), dtype=_BF16, device=dev)
         self.ring_v = torch.empty_like(self.ring_k)
         self.slot_frame = torch.empty((max(window_frames, 1),), dtype=torch.int32, device=dev)

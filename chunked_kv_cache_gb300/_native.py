@@ -29,7 +29,7 @@ EXPORTS = (
     "sr_device_error_status", "sr_debug_wait_timeout", "sr_status_string", "sr_workspace_bytes",
     "sr_chunk_attention_noalloc", "sr_plan_chunk", "sr_rope3d_qk_frames", "sr_chunk_attention_frames",
     "sr_cache_commit_frames", "sr_window_attention", "sr_rope3d_qk_at", "sr_rope3d_qk_dev",
-    "sr_chunk_attention_dev", "sr_cache_commit_dev",
+    "sr_chunk_attention_dev", "sr_cache_commit_dev", "sr_window_count", "sr_plan_window",
 )
 
 
@@ -59,6 +59,11 @@ class SrChunkPlan(ctypes.Structure):
         ("first_frame", ctypes.c_int32), ("n_frames", ctypes.c_int32),
         ("hist_frames", ctypes.c_int32), ("sink_frames", ctypes.c_int32),
     ]
+
+
+class SrWindow(ctypes.Structure):
+    _fields_ = [("row0", ctypes.c_int32), ("col0", ctypes.c_int32), ("rows", ctypes.c_int32),
+                ("cols", ctypes.c_int32)]
 
 
 class SrError(RuntimeError):
@@ -97,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.sr_rope3d_qk_dev.argtypes = [vp, i32, vp, vp, vp]
         L.sr_chunk_attention_dev.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.sr_cache_commit_dev.argtypes = [vp, i32, vp, vp, vp]
+        L.sr_window_count.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32)]
+        L.sr_plan_window.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(SrWindow)]
         L.sr_chunk_attention_batch.argtypes = [ctypes.POINTER(vp), i32, i32, vp, vp, vp,
                                                ctypes.POINTER(i64), vp, vp, vp]
         L.sr_device_error_status.argtypes = [i32]
@@ -199,6 +206,20 @@ def sr_chunk_attention_dev(handle: int, step: int, n_frames: int, hist_frames: i
 
 def sr_cache_commit_dev(handle: int, n_frames: int, k_raw: int, v: int, stream: int) -> None:
     _check(lib().sr_cache_commit_dev(handle, int(n_frames), k_raw, v, stream or None), "sr_cache_commit_dev")
+
+
+def sr_window_count(grid_h: int, grid_w: int, window: int, shifted: bool) -> int:
+    n = ctypes.c_int32()
+    _check(lib().sr_window_count(int(grid_h), int(grid_w), int(window), 1 if shifted else 0, ctypes.byref(n)),
+           "sr_window_count")
+    return n.value
+
+
+def sr_plan_window(grid_h: int, grid_w: int, window: int, shifted: bool, index: int) -> SrWindow:
+    out = SrWindow()
+    _check(lib().sr_plan_window(int(grid_h), int(grid_w), int(window), 1 if shifted else 0, int(index),
+                                ctypes.byref(out)), "sr_plan_window")
+    return out
 
 
 def sr_chunk_attention_noalloc(handle: int, step: int, q: int, k: int, v: int, o: int, lse: int,

@@ -767,6 +767,45 @@ sr_status sr_plan_chunk(int32_t c, int32_t bootstrap_units, int32_t chunk_units,
   return SR_OK;
 }
 
+// Cuts of one axis of n tokens into windows of `w` starting at offset `off`
+// (a first window of off tokens when off > 0): the i-th window's start and size.
+static int32_t axis_windows(int32_t n, int32_t w, int32_t off) { return off == 0 ? (n + w - 1) / w : 1 + (n - off + w - 1) / w; }
+static void axis_window(int32_t n, int32_t w, int32_t off, int32_t i, int32_t& start, int32_t& size) {
+  int32_t a, b;
+  if (off == 0) {
+    a = i * w;
+    b = a + w;
+  } else {
+    a = i == 0 ? 0 : off + (i - 1) * w;
+    b = i == 0 ? off : a + w;
+  }
+  start = a;
+  size = std::min(b, n) - a;
+}
+
+static bool window_args_ok(int32_t gh, int32_t gw, int32_t window, int32_t shifted) {
+  return gh >= 1 && gw >= 1 && window >= 2 && window <= 4096 && (shifted == 0 || shifted == 1) &&
+         gh <= (1 << 20) && gw <= (1 << 20) && !(shifted && (window / 2 >= gh || window / 2 >= gw));
+}
+
+sr_status sr_window_count(int32_t grid_h, int32_t grid_w, int32_t window, int32_t shifted, int32_t* count) {
+  if (!count || !window_args_ok(grid_h, grid_w, window, shifted)) return SR_ERR_INVALID_ARG;
+  const int32_t off = shifted ? window / 2 : 0;
+  *count = axis_windows(grid_h, window, off) * axis_windows(grid_w, window, off);
+  return SR_OK;
+}
+
+sr_status sr_plan_window(int32_t grid_h, int32_t grid_w, int32_t window, int32_t shifted, int32_t index,
+                         sr_window* out) {
+  if (!out || !window_args_ok(grid_h, grid_w, window, shifted)) return SR_ERR_INVALID_ARG;
+  const int32_t off = shifted ? window / 2 : 0;
+  const int32_t nr = axis_windows(grid_h, window, off), nc = axis_windows(grid_w, window, off);
+  if (index < 0 || index >= nr * nc) return SR_ERR_INVALID_ARG;
+  axis_window(grid_h, window, off, index / nc, out->row0, out->rows);
+  axis_window(grid_w, window, off, index % nc, out->col0, out->cols);
+  return SR_OK;
+}
+
 sr_status sr_session_free(sr_session* s) {
   delete s;
   return SR_OK;

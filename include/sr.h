@@ -311,6 +311,28 @@ SR_API sr_status sr_chunk_attention_dev(sr_session* s, int32_t step, int32_t n_f
 SR_API sr_status sr_cache_commit_dev(sr_session* s, int32_t n_frames, const void* k_raw, const void* v,
                                      void* stream);
 
+/*
+ * Window partition of the pages' streaming decoder ([H3 page] 3.2 Iteration 2
+ * "Space": attention within non-overlapping windows of window x window tokens, every
+ * other layer shifted by half a window; Iteration 3 item 4: each window is one short
+ * variable-length sequence, padding positions left out). Host-only arithmetic.
+ * A frame of grid_h x grid_w tokens is cut at rows/columns shift - window, shift,
+ * shift + window, ... (shift = 0 for the plain layers, window / 2 for the shifted ones)
+ * and clipped to the frame, so edge windows are smaller. Windows are numbered row
+ * by row. sr_window_count gives their number; sr_plan_window fills *out for window
+ * `index` (its first token row and column and its size). Each window then attends,
+ * per head, over the global tokens U its cached frames U its chunk frames: with this
+ * library, one session per window (grid = the window's size, the global tokens as a
+ * shared bank), batched by sr_chunk_attention_batch.
+ */
+typedef struct {
+  int32_t row0, col0;      /* first token row and column of the window in the frame */
+  int32_t rows, cols;      /* its size (clipped at the frame edges) */
+} sr_window;
+SR_API sr_status sr_window_count(int32_t grid_h, int32_t grid_w, int32_t window, int32_t shifted, int32_t* count);
+SR_API sr_status sr_plan_window(int32_t grid_h, int32_t grid_w, int32_t window, int32_t shifted, int32_t index,
+                                sr_window* out);
+
 /* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
 SR_API sr_status sr_device_error_status(int32_t err_word_value);
 

@@ -47,3 +47,27 @@ def test_frames_calls_reject_bad_counts_without_a_gpu(sr):
         N.sr_chunk_attention_frames(0, 0, 3, -1, 16, 16, 16, 16, 0, 0)
     with pytest.raises(N.SrError):
         N.sr_cache_commit_frames(0, 3, 16, 16, 0)
+
+
+@pytest.mark.parametrize("gh,gw,window", [(45, 80, 16), (40, 40, 16), (48, 84, 16), (10, 7, 4), (16, 16, 16)])
+@pytest.mark.parametrize("shifted", [False, True])
+def test_c_window_planner_matches_oracle(sr, gh, gw, window, shifted):
+    from chunked_kv_cache_gb300 import _native as N
+    from oracle.decoder import window_partition
+    want = window_partition(gh, gw, window, shifted)
+    n = N.sr_window_count(gh, gw, window, shifted)
+    assert n == len(want)
+    got = [N.sr_plan_window(gh, gw, window, shifted, i) for i in range(n)]
+    assert [(w.row0, w.col0, w.rows, w.cols) for w in got] == want
+
+
+def test_c_window_planner_rejects_invalid(sr):
+    import ctypes
+    from chunked_kv_cache_gb300 import _native as N
+    for args in [(0, 8, 4, 0), (8, 8, 1, 0), (2, 8, 8, 1)]:
+        with pytest.raises(N.SrError):
+            N.sr_window_count(*args)
+    n = ctypes.c_int32()
+    assert N.lib().sr_window_count(8, 8, 4, 2, ctypes.byref(n)) == N.SR_ERR_INVALID_ARG   # shifted must be 0 or 1
+    with pytest.raises(N.SrError):
+        N.sr_plan_window(8, 8, 4, 0, 4)
