@@ -70,6 +70,9 @@ struct Cfg {
   // more stage (each iteration then needs four tiles: two K, two V).
   static constexpr int kStages = D == 128 ? 5 : 6;
   static constexpr int kStagesSplit = kStages + 1;
+  // K/V travel in stage pairs (a K slot and a V slot behind one barrier)
+  static constexpr int kPairs = kStages / 2;
+  static constexpr int kPairsSplit = kStagesSplit / 2;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemKV = kStages * kTileBytes;
   static constexpr int kSmemBar = 2048;
@@ -249,49 +252,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_2d(sQ + t * C::kTileBytes + a * C::kAtomBytes, &p.qmap, &bars->q_full,
                       head * D + a * 64, S.q_row0 + q_local0 + t * BM, pol_q);
-      int idx = 0;
+      // K/V tiles travel in stage pairs behind one barrier: pair p is the
+      // slots 2p (a K tile) and 2p+1 (a V tile); the extra split-mode slot is
+      // the second Q slot.
+      const int npair = wk.split ? C::kPairsSplit : C::kPairs;
+      int q = 0;   // pair loads issued so far
       bool ok = true;
-      const int nst = wk.split ? C::kStagesSplit : C::kStages;
-      auto load = [&](bool is_v, int j) {
-        if (!ok) return;
-        const int stage = idx % nst;
-        if (idx >= nst && !wait_bounded(&bars->kv_empty[stage], ((idx / nst) - 1) & 1, wc, 1)) {
-          ok = false;
-          return;
-        }
+      auto slot_ptr = [&](int slot) -> uint8_t* {
+        return slot < C::kStages ? sKV + slot * C::kTileBytes : sQ + C::kTileBytes;
+      };
+      auto issue = [&](int j, bool is_v, int slot, uint64_t* bar) {
         int seg, row0;
         tm.locate(j, seg, row0);
         const CUtensorMap* map = is_v ? &S.vmap[seg] : &S.kmap[seg];
-        mbar_arrive_expect_tx(&bars->kv_full[stage], C::kTileBytes);
-        uint8_t* dst = stage < C::kStages ? sKV + stage * C::kTileBytes : sQ + C::kTileBytes;
+        uint8_t* dst = slot_ptr(slot);
         for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_2d(dst + a * C::kAtomBytes, map, &bars->kv_full[stage], head * D + a * 64, tm.base[seg] + row0,
-                      pol_kv);
-        ++idx;
+          tma_load_2d(dst + a * C::kAtomBytes, map, bar, head * D + a * 64, tm.base[seg] + row0, pol_kv);
+      };
+      // one pair: key tile kj (if >= 0) and value tile vj (if >= 0)
+      auto load_pair = [&](int kj, int vj) {
+        if (!ok) return;
+        const int pr = q % npair;
+        if (q >= npair && !wait_bounded(&bars->kv_empty[pr], ((q / npair) - 1) & 1, wc, 1)) {
+          ok = false;
+          return;
+        }
+        mbar_arrive_expect_tx(&bars->kv_full[pr], ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
+        if (kj >= 0) issue(kj, false, 2 * pr, &bars->kv_full[pr]);
+        if (vj >= 0) issue(vj, true, 2 * pr + 1, &bars->kv_full[pr]);
+        ++q;
       };
       const int n_it = wk.iters();
       if (!wk.split) {
-        // shared mode, per iteration: K_i, then V_{i-1}
-        for (int i = 0; i < n_it && ok; ++i) {
-          load(false, i);
-          if (i > 0) load(true, i - 1);
-        }
-        load(true, n_it - 1);
+        // shared mode, iteration i: K_i (the S MMAs of both tiles) and V_{i-1}
+        for (int i = 0; i <= n_it && ok; ++i) load_pair(i < n_it ? i : -1, i > 0 ? i - 1 : -1);
       } else {
-        // split mode, in the order the MMAs consume them: per iteration and
-        // tile t, V(t, i-1) then K(t, i); every load then reuses a stage that
-        // was freed at least an iteration before it is needed
+        // split mode, iteration i and tile t: K(t, i) and V(t, i-1), tile 0 first
         for (int i = 0; i <= n_it && ok; ++i)
           for (int t = 0; t < 2; ++t) {
-            if (i > 0 && i - 1 < wk.count(t)) load(true, wk.kv(t, i - 1));
-            if (i < wk.count(t)) load(false, wk.kv(t, i));
+            const bool kq = i < wk.count(t), vq = i > 0 && i - 1 < wk.count(t);
+            if (kq || vq) load_pair(kq ? wk.kv(t, i) : -1, vq ? wk.kv(t, i - 1) : -1);
           }
       }
       if (!ok || bars->abort) {
         // let every copy this CTA started land before shared memory is released
         wait_drain(&bars->q_full, 0, p.timeout_ns);
-        for (int k = max(0, idx - nst); k < idx; ++k)
-          wait_drain(&bars->kv_full[k % nst], (k / nst) & 1, p.timeout_ns);
+        for (int k = max(0, q - npair); k < q; ++k)
+          wait_drain(&bars->kv_full[k % npair], (k / npair) & 1, p.timeout_ns);
       }
     } else if (warp == kMmaWarp) {
       // ---------------------------------------------------------- MMA issuer
@@ -303,19 +310,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       bool ok = __all_sync(0xffffffffu, wait_bounded(&bars->q_full, 0, wc, 2));
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
-      // Position in the producer's load sequence: stage and phase parity of
-      // the next load, advanced by counters (no division on this warp).
-      const int nst = wk.split ? C::kStagesSplit : C::kStages;
-      int st = 0;
+      // Position in the producer's sequence of stage pairs: pair and phase
+      // parity of the next one, advanced by counters (no division on this warp).
+      const int npair = wk.split ? C::kPairsSplit : C::kPairs;
+      int pc = 0;
       uint32_t ph = 0;
-      auto take = [&]() -> int {   // wait for the next load; its stage
-        const int s0 = st;
-        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->kv_full[s0], ph, wc, 3));
-        if (++st == nst) {
-          st = 0;
+      auto take = [&]() -> int {   // wait for the next pair; returns its index
+        const int p0 = pc;
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->kv_full[p0], ph, wc, 3));
+        if (++pc == npair) {
+          pc = 0;
           ph ^= 1u;
         }
-        return s0;
+        return p0;
       };
       auto wait_p = [&](int t, int it) {   // softmax group t has written P_t of iteration it
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->p_full[t], it & 1, wc, 4));
@@ -354,94 +361,93 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         // and last iterations are peeled off, so the body branches only to
         // leave on an abort.
         const int n = wk.n;
-        // iteration 0: S_0 of both tiles
-        const int k0 = take();
+        // iteration 0: S_0 of both tiles (pair 0 holds K_0 only)
+        const int p0 = take();
         if (ok) {
           tc_fence_after();
-          qk(0, k0);
+          qk(0, 2 * p0);
           tc_commit_w(&bars->s_full[0], leader);
-          qk(1, k0);
+          qk(1, 2 * p0);
           tc_commit_w(&bars->s_full[1], leader);
-          tc_commit_w(&bars->kv_empty[k0], leader);
+          tc_commit_w(&bars->kv_empty[p0], leader);
           issued_any = true;
         }
-        // iterations 1 .. n-1: PV_{i-1} and S_i of both tiles. The two takes
-        // come first, while the warp would otherwise be waiting for softmax
-        // group 0; between S0_i and PV1_{i-1} there is only that group's wait.
+        // iterations 1 .. n-1: PV_{i-1} and S_i of both tiles from one pair
+        // (K_i, V_{i-1}). Its wait comes first, while the warp would otherwise
+        // be waiting for softmax group 0; between S0_i and PV1_{i-1} there is
+        // only that group's wait.
         for (int i = 1; i < n && ok; ++i) {
-          const int ki = take();
-          const int vi = take();
+          const int pi = take();
           tc_fence_after();
           wait_p(0, i - 1);
           if (!ok) break;
-          pv(0, vi, i > 1);
-          qk(0, ki);
+          pv(0, 2 * pi + 1, i > 1);
+          qk(0, 2 * pi);
           tc_commit_w(&bars->s_full[0], leader);
           wait_p(1, i - 1);
           if (!ok) break;
-          pv(1, vi, i > 1);
-          qk(1, ki);
+          pv(1, 2 * pi + 1, i > 1);
+          qk(1, 2 * pi);
           tc_commit_w(&bars->s_full[1], leader);
-          tc_commit_w(&bars->kv_empty[vi], leader);
-          tc_commit_w(&bars->kv_empty[ki], leader);
+          tc_commit_w(&bars->kv_empty[pi], leader);
         }
-        // last: PV_{n-1} of both tiles
+        // last: PV_{n-1} of both tiles (the last pair holds V_{n-1} only)
         if (ok) {
-          const int vl = take();
+          const int pl = take();
           tc_fence_after();
           wait_p(0, n - 1);
           if (ok) {
-            pv(0, vl, n > 1);
+            pv(0, 2 * pl + 1, n > 1);
             tc_commit_w(&bars->o_done[0], leader);
             wait_p(1, n - 1);
           }
           if (ok) {
-            pv(1, vl, n > 1);
+            pv(1, 2 * pl + 1, n > 1);
             tc_commit_w(&bars->o_done[1], leader);
-            tc_commit_w(&bars->kv_empty[vl], leader);
+            tc_commit_w(&bars->kv_empty[pl], leader);
           }
         }
       } else {
         // Split mode (a single-tile last block): tile 0 walks c0 key tiles,
-        // tile 1 the next c1 (c0 - c1 is 0 or 1). The producer loads, per
-        // iteration i and tile t, V(t, i-1) then K(t, i); tile 1's waits come
-        // after tile 0's MMAs are queued.
+        // tile 1 the next c1 (c0 - c1 is 0 or 1). Iteration i takes, per tile
+        // t, one pair holding K(t, i) and V(t, i-1); tile 1's wait comes after
+        // tile 0's MMAs are queued.
         const int c0 = wk.count(0), c1 = wk.count(1);
         for (int i = 0; i <= c0 && ok; ++i) {
           const bool p0 = i > 0 && i - 1 < c0, q0 = i < c0;
-          const int v0 = p0 ? take() : 0;
-          const int k0 = q0 ? take() : 0;
-          if (!ok) break;
-          tc_fence_after();
-          if (p0) {
-            wait_p(0, i - 1);
+          if (p0 || q0) {
+            const int pr = take();   // K(0, i) and V(0, i-1)
             if (!ok) break;
-            pv(0, v0, i > 1);
-            if (i == c0) tc_commit_w(&bars->o_done[0], leader);
-            tc_commit_w(&bars->kv_empty[v0], leader);
-          }
-          if (q0) {
-            qk(0, k0);
-            tc_commit_w(&bars->s_full[0], leader);
-            tc_commit_w(&bars->kv_empty[k0], leader);
-            issued_any = true;
+            tc_fence_after();
+            if (p0) {
+              wait_p(0, i - 1);
+              if (!ok) break;
+              pv(0, 2 * pr + 1, i > 1);
+              if (i == c0) tc_commit_w(&bars->o_done[0], leader);
+            }
+            if (q0) {
+              qk(0, 2 * pr);
+              tc_commit_w(&bars->s_full[0], leader);
+              issued_any = true;
+            }
+            tc_commit_w(&bars->kv_empty[pr], leader);
           }
           const bool p1 = i > 0 && i - 1 < c1, q1 = i < c1;
-          const int v1 = p1 ? take() : 0;
-          const int k1 = q1 ? take() : 0;
-          if (!ok) break;
-          tc_fence_after();
-          if (p1) {
-            wait_p(1, i - 1);
+          if (p1 || q1) {
+            const int pr = take();   // K(1, i) and V(1, i-1)
             if (!ok) break;
-            pv(1, v1, i > 1);
-            if (i == c1) tc_commit_w(&bars->o_done[1], leader);
-            tc_commit_w(&bars->kv_empty[v1], leader);
-          }
-          if (q1) {
-            qk(1, k1);
-            tc_commit_w(&bars->s_full[1], leader);
-            tc_commit_w(&bars->kv_empty[k1], leader);
+            tc_fence_after();
+            if (p1) {
+              wait_p(1, i - 1);
+              if (!ok) break;
+              pv(1, 2 * pr + 1, i > 1);
+              if (i == c1) tc_commit_w(&bars->o_done[1], leader);
+            }
+            if (q1) {
+              qk(1, 2 * pr);
+              tc_commit_w(&bars->s_full[1], leader);
+            }
+            tc_commit_w(&bars->kv_empty[pr], leader);
           }
         }
       }
