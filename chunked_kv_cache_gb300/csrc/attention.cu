@@ -633,7 +633,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     if (writer && parts > 1) {
       // Every part has published its rows; the last part to arrive merges them.
       // The counter holds (epoch << 4 | arrivals): raising it to this call's
-      // epoch first discards any count left by an earlier, aborted call.
+      // epoch first discards any count left by an earlier, aborted call. The
+      // last part clears it once every part has arrived, so that a replay of
+      // the same launch (a CUDA graph repeats the epoch) starts from zero.
       __threadfence();
       named_sync(2, BM);
       if (threadIdx.x == 0) {
@@ -643,6 +645,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           atomicMax(ctr, S.epoch << 4);
           const int old = atomicAdd(ctr, 1);
           last = ((old >> 4) == S.epoch) && ((old & 15) == parts - 1);
+          if (last) atomicExch(ctr, 0);
         }
         bars->last = last;
       }

@@ -22,6 +22,7 @@
 #include <functional>
 #include <mutex>
 #include <new>
+#include <queue>
 #include <vector>
 
 #include "sr.h"
@@ -254,17 +255,27 @@ int64_t key_tiles(const sr_session* s, const ChunkView& view) {
   return n;
 }
 
-// How many CTAs share the key range of each single-tile last block.
+int sm_count() {
+  static int counts[64];
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return 152;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+// How many CTAs share the key range of each single-tile last block. Units are
+// dispatched in order (full blocks, then last-block parts) to whichever SM
+// frees up first, one CTA per SM; simulate that for 1..4 parts and keep the
+// shortest makespan, ties going to more parts. Costs in key-tile iterations
+// of a full block, measured on GB300: a full block walks all its key tiles; a
+// last-block part walks its share in split mode, half the tiles per query
+// tile at 1.33x the cost of a full-block iteration, plus about half an
+// iteration of set-up and, when split, half an iteration of merge.
 int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* order, int n) {
-  // The single-tile last blocks run after every full block (longest first)
-  // and land on the few SMs the last wave of full blocks leaves free; cutting
-  // their key ranges into parts spreads them over more SMs and shortens the
-  // piece that finishes last. Measured on GB300 (832x480 and 720p chunks),
-  // every split of 2-8 parts beat no split and 4 parts or more were within
-  // 1% of each other, while the merge costs little. So: as many parts as the
-  // workspace holds, as long as each part keeps at least kMinTilesPerPart
-  // key tiles (8 iterations of the two-tile split walk).
-  constexpr int64_t kMinTilesPerPart = 16;
   const int forced = ss[0]->cfg.tail_split;
   int64_t min_kv = INT64_MAX;
   for (int r = 0; r < n; ++r) {
@@ -276,7 +287,41 @@ int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* 
   }
   const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, min_kv));
   if (forced > 0) return std::max(1, std::min(forced, cap));
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cap, min_kv / kMinTilesPerPart)));
+  const int G = sm_count();
+  int best = 1;
+  double best_t = 0;
+  for (int k = 1; k <= cap; ++k) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int g = 0; g < G; ++g) free_at.push(0.0);
+    auto run = [&](double cost) {
+      const double t0 = free_at.top();
+      free_at.pop();
+      free_at.push(t0 + cost);
+    };
+    for (int r = 0; r < n; ++r) {
+      const sr_session* s = ss[order[r]];
+      const ChunkView& view = views[order[r]];
+      const int64_t units = static_cast<int64_t>(s->cfg.n_heads) * ((view.lq + 255) / 256 - 1);
+      const double cost = static_cast<double>(key_tiles(s, view));
+      for (int64_t u = 0; u < units; ++u) run(cost);
+    }
+    for (int r = 0; r < n; ++r) {
+      const sr_session* s = ss[order[r]];
+      const double tiles = static_cast<double>(key_tiles(s, views[order[r]]));
+      const double part = std::ceil(std::ceil(tiles / k) / 2.0) * 1.33 + 0.5 + (k > 1 ? 0.5 : 0.0);
+      for (int64_t u = 0; u < static_cast<int64_t>(s->cfg.n_heads) * k; ++u) run(part);
+    }
+    double t = 0;
+    while (!free_at.empty()) {
+      t = std::max(t, free_at.top());
+      free_at.pop();
+    }
+    if (k == 1 || t <= best_t * 1.0001) {
+      best = k;
+      best_t = std::min(best_t > 0 ? best_t : t, t);
+    }
+  }
+  return best;
 }
 
 }  // namespace
