@@ -155,6 +155,10 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
 template <int D, int NSESS>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams<NSESS> p) {
   using C = Cfg<D>;
+  // the previous kernel of the stream may still be draining: wait for it
+  // before any global access, then let the next one be scheduled
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -723,19 +727,15 @@ cudaError_t attn_prepare(int head_dim, int nsess_template) {
 cudaError_t launch_attention_1(const AttnParams<1>& p, int head_dim, int n_units, cudaStream_t st) {
   if (n_units == 0) return cudaSuccess;
   if (head_dim == 128)
-    attn_kernel<128, 1><<<n_units, kAttnThreads, Cfg<128>::kSmemBytes, st>>>(p);
-  else
-    attn_kernel<64, 1><<<n_units, kAttnThreads, Cfg<64>::kSmemBytes, st>>>(p);
-  return cudaGetLastError();
+    return launch_dependent(attn_kernel<128, 1>, n_units, kAttnThreads, Cfg<128>::kSmemBytes, st, p);
+  return launch_dependent(attn_kernel<64, 1>, n_units, kAttnThreads, Cfg<64>::kSmemBytes, st, p);
 }
 
 cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim, int n_units, cudaStream_t st) {
   if (n_units == 0) return cudaSuccess;
   if (head_dim == 128)
-    attn_kernel<128, kAttnMaxBatch><<<n_units, kAttnThreads, Cfg<128>::kSmemBytes, st>>>(p);
-  else
-    attn_kernel<64, kAttnMaxBatch><<<n_units, kAttnThreads, Cfg<64>::kSmemBytes, st>>>(p);
-  return cudaGetLastError();
+    return launch_dependent(attn_kernel<128, kAttnMaxBatch>, n_units, kAttnThreads, Cfg<128>::kSmemBytes, st, p);
+  return launch_dependent(attn_kernel<64, kAttnMaxBatch>, n_units, kAttnThreads, Cfg<64>::kSmemBytes, st, p);
 }
 
 // ---------------------------------------------------------------- diagnostics

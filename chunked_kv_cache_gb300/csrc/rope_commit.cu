@@ -19,6 +19,7 @@
 // once.
 #include <cuda_bf16.h>
 
+#include "sr_device.cuh"
 #include "sr_kernels.h"
 
 namespace sr {
@@ -43,6 +44,8 @@ template <int D>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, int tokens_per_cta) {
   constexpr int kPairs = D / 2;
   constexpr int kVecPerHead = D / 8;
+  grid_dep_wait();   // the previous kernel of the stream may still be draining
+  grid_dep_launch_dependents();
   extern __shared__ float2 smem_rope[];
   float2* cs_table = smem_rope;                                               // [tokens_per_cta][D/2]
   int32_t* dst_row = reinterpret_cast<int32_t*>(smem_rope + tokens_per_cta * kPairs);   // [tokens_per_cta]
@@ -171,16 +174,15 @@ cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st) {
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    rope_kernel<128><<<static_cast<unsigned>(grid), kRopeThreads, smem, st>>>(p, tokens_per_cta);
+    return launch_dependent(rope_kernel<128>, static_cast<unsigned>(grid), kRopeThreads, smem, st, p, tokens_per_cta);
   } else {
     if (smem > 48 * 1024) {
       cudaError_t e = cudaFuncSetAttribute(rope_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    rope_kernel<64><<<static_cast<unsigned>(grid), kRopeThreads, smem, st>>>(p, tokens_per_cta);
+    return launch_dependent(rope_kernel<64>, static_cast<unsigned>(grid), kRopeThreads, smem, st, p, tokens_per_cta);
   }
-  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ small helpers

@@ -21,6 +21,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel launched with programmatic stream serialization may be scheduled
+// while the previous kernel of its stream is still draining. grid_dep_wait()
+// returns once that kernel has completed and its writes are visible (at once
+// when there is no such predecessor), so nothing before it may touch global
+// memory. grid_dep_launch_dependents() lets the next kernel be scheduled once
+// every CTA of this grid has started.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

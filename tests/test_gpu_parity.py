@@ -66,6 +66,39 @@ def test_cache_commit_matches_oracle(config, fill, chunks, clock):
     assert tw.gpu.error_status() == 0
 
 
+ODD_SHAPES = [
+    # (heads, d, grid_h, grid_w, F, W): 16-byte vectors per token 8 .. 80, frames
+    # that do not divide a copy chunk, a single token per frame
+    (1, 64, 5, 7, 3, 4),
+    (5, 128, 7, 9, 2, 3),
+    (3, 64, 1, 1, 2, 5),
+    (2, 128, 13, 29, 2, 2),
+]
+
+
+@pytest.mark.parametrize("H,d,gh,gw,F,W", ODD_SHAPES)
+def test_rope_and_commit_odd_shapes(H, d, gh, gw, F, W):
+    shape = syn.Shape(f"odd {H}x{d} {gh}x{gw}", H, d, gh, gw, F, W, 16)
+    tw = Twin(shape, 1, fill=0, t_clock0=5)
+    for c in range(4):   # past one wrap of the ring
+        x = syn.chunk_inputs(shape, 1, chunk=200 + c)
+        q, k = to_dev(x.q[0], tw.dev), to_dev(x.k[0], tw.dev)
+        tw.gpu.rope3d_qk(q, k)
+        qo, ko = tw.ora.rope3d_qk(x.q[0], x.k[0])
+        assert_rotated_close(syn.torch_to_bits(q), qo, "q")
+        assert_rotated_close(syn.torch_to_bits(k), ko, "k")
+        tw.commit(x)
+        torch.cuda.synchronize()
+        assert tw.gpu.frames == tw.ora.n_committed
+        assert np.array_equal(tw.gpu.slot_frame.cpu().numpy(), tw.ora.ring.slot_frame.astype(np.int32))
+    rk, rv = tw.ring_bits()
+    ok_, ov_ = tw.ora.ring_bits()
+    occupied = np.repeat(tw.ora.ring.slot_frame >= 0, shape.tokens_per_frame)
+    assert np.array_equal(rv[occupied], ov_[occupied])
+    assert_rotated_close(rk[occupied], ok_[occupied], "ring K")
+    assert tw.gpu.error_status() == 0
+
+
 # ------------------------------------------------------------------ attention
 
 @pytest.mark.parametrize("fill", [0, 1, 3, 4])
