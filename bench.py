@@ -279,49 +279,57 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def hbm_kernel_times(sessions, shape, reps: int = 16):
+def hbm_kernel_times(sessions, shape, reps: int = 16, rounds: int = 7):
     """Mean ms per launch of RoPE-3D (mode 0) and of the ring commit, each timed
-    over `reps` back-to-back launches between one pair of events."""
+    over `reps` back-to-back launches between one pair of events; the median of
+    `rounds` such timings."""
     pairs = [(x["q"][st], x["k"][st]) for _, x in sessions for st in range(shape.n_steps)]
     pairs += [(x["clean_k"], x["clean_v"]) for _, x in sessions]
     out = []
     for kind in ("rope", "commit"):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        ev0.record()
-        for i in range(reps):
-            if kind == "rope":
-                s = sessions[i % len(sessions)][0]
-                q, k = pairs[i % len(pairs)]
-                s.rope3d_qk(q, k)
-            else:
-                s, x = sessions[i % len(sessions)]
-                s.cache_commit(x["clean_k"], x["clean_v"])
-        ev1.record()
-        torch.cuda.synchronize()
-        out.append(ev0.elapsed_time(ev1) / reps)
+        times = []
+        for _ in range(rounds):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            ev0.record()
+            for i in range(reps):
+                if kind == "rope":
+                    s = sessions[i % len(sessions)][0]
+                    q, k = pairs[i % len(pairs)]
+                    s.rope3d_qk(q, k)
+                else:
+                    s, x = sessions[i % len(sessions)]
+                    s.cache_commit(x["clean_k"], x["clean_v"])
+            ev1.record()
+            torch.cuda.synchronize()
+            times.append(ev0.elapsed_time(ev1) / reps)
+        out.append(statistics.median(times))
     return out[0], out[1]
 
 
 def run_e2e(shape, args, dev, sess):
     """Same chunk through the public API with the step's inputs copied in from
-    pinned host memory and both steps' outputs copied back, every step. The
-    copies run on a second stream, double-buffered: chunk i+1's inputs go up
-    while chunk i computes, and chunk i's outputs come back while chunk i+1
-    computes; every chunk still moves all of its own inputs and outputs inside
-    the timed region."""
-    n = max(3, min(args.steps, 10))
+    pinned host memory and both steps' outputs copied back, every step. Uploads
+    and read-backs run on two more streams (the host link is full duplex), over
+    three buffer sets: chunk i+2's inputs go up and chunk i-1's outputs come
+    back while chunk i computes; every chunk still moves all of its own inputs
+    and outputs inside the timed region, which starts before the first upload
+    and ends after the last read-back."""
+    n = max(3, args.steps)
+    nbuf = 3
     dims = (shape.lq, shape.n_heads, shape.head_dim)
     g = torch.Generator().manual_seed(1234)
     n_in = 3 * shape.n_steps + 2
     host_in = [[torch.randn(dims, generator=g).to(torch.bfloat16).pin_memory() for _ in range(n_in)]
-               for _ in range(2)]
+               for _ in range(nbuf)]
     host_out = [[torch.empty(dims, dtype=torch.bfloat16).pin_memory() for _ in range(shape.n_steps)]
-                for _ in range(2)]
-    dev_in = [[torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in range(n_in)] for _ in range(2)]
-    dev_out = [[torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in range(shape.n_steps)] for _ in range(2)]
+                for _ in range(nbuf)]
+    dev_in = [[torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in range(n_in)] for _ in range(nbuf)]
+    dev_out = [[torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in range(shape.n_steps)]
+               for _ in range(nbuf)]
     comp = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
+    h2d = torch.cuda.Stream(dev)
+    d2h = torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
 
     def run(chunks):
@@ -329,35 +337,36 @@ def run_e2e(shape, args, dev, sess):
         done = [ev() for _ in range(chunks)]     # chunk i computed
         down = [ev() for _ in range(chunks)]     # chunk i's outputs are back on the host
         def upload(i):
-            b = i % 2
-            with torch.cuda.stream(copy):
-                if i >= 2:
-                    copy.wait_event(done[i - 2])   # buffer set b is free again
+            b = i % nbuf
+            with torch.cuda.stream(h2d):
+                if i >= nbuf:
+                    h2d.wait_event(done[i - nbuf])   # buffer set b is free again
                 for h, d in zip(host_in[b], dev_in[b]):
                     d.copy_(h, non_blocking=True)
-                up[i].record(copy)
-        upload(0)
+                up[i].record(h2d)
+        for i in range(min(nbuf - 1, chunks)):
+            upload(i)
         for i in range(chunks):
-            b = i % 2
-            if i + 1 < chunks:
-                upload(i + 1)
+            b = i % nbuf
+            if i + nbuf - 1 < chunks:
+                upload(i + nbuf - 1)
             comp.wait_event(up[i])
-            if i >= 2:
-                comp.wait_event(down[i - 2])      # its output buffers have been read back
+            if i >= nbuf:
+                comp.wait_event(down[i - nbuf])      # its output buffers have been read back
             for st in range(shape.n_steps):
                 q, k, v = dev_in[b][3 * st], dev_in[b][3 * st + 1], dev_in[b][3 * st + 2]
                 sess.rope3d_qk(q, k)
                 sess.chunk_attention(st, q, k, v, out=dev_out[b][st])
             sess.cache_commit(dev_in[b][-2], dev_in[b][-1])
             done[i].record(comp)
-            with torch.cuda.stream(copy):
-                copy.wait_event(done[i])
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(done[i])
                 for d, h in zip(dev_out[b], host_out[b]):
                     h.copy_(d, non_blocking=True)
-                down[i].record(copy)
+                down[i].record(d2h)
         torch.cuda.synchronize()
 
-    run(2)
+    run(3)
     t = time.perf_counter()
     run(n)
     sec = time.perf_counter() - t
