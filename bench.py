@@ -408,6 +408,32 @@ def cpu_baseline(shape, args, budget_s: float = 12.0):
                       f"({shape.lq} queries x {lk} keys, float64 numpy), {t_used:.1f} s"}
 
 
+def _oracle_attention_rate(parts, d, budget_s: float = 6.0):
+    """The float64 oracle's attention on the host cores, one head at a time over
+    the (queries, keys) shapes in `parts`, round robin until the time budget is
+    used (at least one head each). Returns (flop/s, heads done, seconds)."""
+    from oracle import attention
+    g = np.random.default_rng(0)
+    done, used, flops = 0, 0.0, 0.0
+    while done < len(parts) or used < budget_s:
+        lq, lk = parts[done % len(parts)]
+        q = g.standard_normal((lq, 1, d))
+        k = g.standard_normal((lk, 1, d))
+        v = g.standard_normal((lk, 1, d))
+        t = time.perf_counter()
+        attention(q, k, v, 1.0 / math.sqrt(d))
+        used += time.perf_counter() - t
+        flops += 4.0 * lq * lk * d
+        done += 1
+    return flops / used, done, used
+
+
+def _oracle_line(rate, done, used, what, value=None, unit=UNIT):
+    """cpu_baseline object: TFLOP/s unless a converted value and unit are given."""
+    return {"value": round(rate / 1e12, 5) if value is None else value, "unit": unit, "cores": os.cpu_count(),
+            "kind": "oracle", "sample": f"{done} heads of {what} (float64 numpy), {used:.1f} s"}
+
+
 def run_reference(args):
     """Reference arm: the float64 oracle on the host cores, each step a bounded
     sample (one head of one denoising step, full window) of the same workload."""
@@ -542,6 +568,8 @@ def run_rhythm(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4), "kernel": "attn_kernel (sr_chunk_attention_frames)",
                      "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "cpu_baseline": _oracle_line(*_oracle_attention_rate([(e["lq"], e["lk"]) for e in per_kind.values()], d),
+                                     "one denoising step of the 3- and 2-latent chunks, alternately"),
         "clocks": clk.summary(),
         "gpu_launches": 5 * steps,
     }
@@ -642,6 +670,8 @@ def run_window(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4), "kernel": "attn_kernel (sr_window_attention)",
                      "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "cpu_baseline": _oracle_line(*_oracle_attention_rate([(M, S + M)], d),
+                                     f"one denoising step's window attention ({M} moving rows x {S + M} keys)"),
         "clocks": clk.summary(),
         "gpu_launches": 4 * args.steps,
     }
@@ -707,6 +737,10 @@ def run_graph(args):
         results[name] = res
         s.close()
     main = results["832x480"]
+    sh = shapes["832x480"]
+    lk = sh.lk(sh.window_frames)
+    rate, done, used = _oracle_attention_rate([(sh.lq, lk)], sh.head_dim)
+    chunk_ms = sh.n_steps * 4.0 * sh.n_heads * sh.lq * lk * sh.head_dim / rate * 1e3
     out = {
         "metric": "per-chunk time, eager calls vs CUDA-graph replay (device-resident chunk state), 1 GB300",
         "value": main["graph"]["ms_per_chunk"], "unit": "ms/chunk", "higher_is_better": False, "n_gpus": 1,
@@ -714,6 +748,9 @@ def run_graph(args):
         "config": {"workload": "steady state (ring full), one step = one chunk: 2 x (RoPE-3D + chunk attention) + "
                                "ring commit through the *_dev calls; eager vs one graph replay"},
         "shapes": results,
+        "cpu_baseline": _oracle_line(rate, done, used, f"one 832x480 denoising step ({sh.lq} queries x {lk} keys); "
+                                     "ms per chunk extrapolated to all heads and both steps, attention only",
+                                     value=round(chunk_ms, 1), unit="ms/chunk"),
         "gpu_launches": 6 * args.steps,
     }
     print(json.dumps(out), flush=True)
@@ -737,7 +774,7 @@ def run_decoder(args):
     from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
     H, d, G = 16, 128, 5
     grids = {"720p (45x80 tokens)": (45, 80), "768x1344 (48x84 tokens)": (48, 84)}
-    results = {}
+    results, lay_fl = {}, {}
     peak_tf, _, peak_kind = _peaks()
     for gname, (gh, gw) in grids.items():
         for shifted in (False, True):
@@ -763,6 +800,7 @@ def run_decoder(args):
             ms = a.elapsed_time(b) / args.steps
             fl = sum(4.0 * H * s.lq * (G + 6 * s.T) * d for s in lay.sessions)
             full = [s for s in lay.sessions if s.T == 256]
+            lay_fl[f"{gname}, {'shifted' if shifted else 'plain'} layer"] = fl
             results[f"{gname}, {'shifted' if shifted else 'plain'} layer"] = {
                 "windows": len(lay.windows), "full_windows": len(full), "launches": len(lay.groups),
                 "ms_per_layer": round(ms, 4), "tflops": round(fl / (ms / 1e3) / 1e12, 2)}
@@ -770,6 +808,7 @@ def run_decoder(args):
                 raise RuntimeError("device error word set during the bench")
             lay.close()
     key = "768x1344 (48x84 tokens), shifted layer"
+    rate, done, used = _oracle_attention_rate([(512, G + 6 * 256)], d)
     out = {
         "metric": "decoder window attention ms per layer on 1 GB300", "value": results[key]["ms_per_layer"],
         "unit": "ms/layer", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -782,6 +821,9 @@ def run_decoder(args):
         "roofline": {"bound": "tensor", "achieved": results[key]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(results[key]["tflops"] / peak_tf, 4),
                      "kernel": "attn_kernel<128,16> (sr_chunk_attention_batch)", "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "cpu_baseline": _oracle_line(rate, done, used, "one full window (512 queries x 1541 keys); ms per layer "
+                                     "extrapolated to every window and head of the " + key,
+                                     value=round(lay_fl[key] / rate * 1e3, 2), unit="ms/layer"),
         "gpu_launches": sum(v["launches"] for v in results.values()) * args.steps,
     }
     print(json.dumps(out), flush=True)

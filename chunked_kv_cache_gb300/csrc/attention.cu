@@ -133,21 +133,25 @@ template <int NSESS>
 __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, int H, int& si, int& head,
                                             int& qb, int& part) {
   part = 0;
+  si = 0;
   if (u < p.n_full_units) {
-    si = 0;
+    // whole blocks, session by session, the blocks of one head next to each
+    // other (they read the same keys and values, which then come from L2)
 #pragma unroll 1
-    while (si + 1 < p.n_sess && u >= p.sess[si].unit_begin + H * (p.sess[si].nqb - 1)) ++si;
+    while (si + 1 < p.n_sess && u >= p.sess[si].unit_begin + H * p.sess[si].nfull) ++si;
     const int local = u - p.sess[si].unit_begin;
-    const int nf = p.sess[si].nqb - 1;
+    const int nf = p.sess[si].nfull;
     head = local / nf;
     qb = local % nf;
   } else {
-    // every session has H last blocks, each run as tail_split key-range parts
+    // single-tile last blocks (H per session that has them), each run as
+    // tail_split key-range parts
     const int t = u - p.n_full_units;
     const int tail = t / p.tail_split;
     part = t - tail * p.tail_split;
-    si = tail / H;
-    head = tail - si * H;
+#pragma unroll 1
+    while (si + 1 < p.n_sess && tail >= p.sess[si].tail_begin + H * p.sess[si].ntail) ++si;
+    head = tail - p.sess[si].tail_begin;
     qb = p.sess[si].nqb - 1;
   }
 }
@@ -155,9 +159,9 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
 template <int D, int NSESS>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams<NSESS> p) {
   using C = Cfg<D>;
-  // the previous kernel of the stream may still be draining: wait for it
-  // before any global access, then let the next one be scheduled
-  grid_dep_wait();
+  // The previous kernel of the stream may still be draining: the set-up below
+  // touches no global memory until grid_dep_wait(). The next kernel may be
+  // scheduled as soon as every CTA of this grid has started.
   grid_dep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,6 +186,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   if (S.dev_n != nullptr) {
     // The visible ring frames follow the device frame counter: frames n-h ..
     // n-1 in slots (g mod W), one or two row ranges of the whole-ring maps.
+    grid_dep_wait();
     const int64_t n = *S.dev_n;
     const int W = S.ring_W, T = S.ring_T;
     const int v = static_cast<int>(min(n, static_cast<int64_t>(W)));
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_wait();   // returns at once when it already returned above
   const uint32_t tmem = bars->tmem_base;
   const TileMap& tm = bars->tm;
 

@@ -197,7 +197,19 @@ sr_status encode_group(sr::AttnSession& out, const Segment (&seg)[sr::kSegs], in
   out.q_row0 = static_cast<int32_t>(row0);
   out.lq = static_cast<int32_t>(lq);
   out.nqb = static_cast<int32_t>((lq + 255) / 256);
+  const int64_t rem = lq % 256;
+  out.ntail = (rem > 0 && rem <= 128) ? 1 : 0;   // a single-tile last block
+  out.nfull = out.nqb - out.ntail;
   return SR_OK;
+}
+
+// Place a query group's units: its whole blocks after `full` units, its
+// single-tile last blocks after `tails` last-block units (both advance).
+void place_units(sr::AttnSession& g, int n_heads, int& full, int& tails) {
+  g.unit_begin = full;
+  g.tail_begin = tails;
+  full += n_heads * g.nfull;
+  tails += n_heads * g.ntail;
 }
 
 const char* bank_ptr(const void* bank, const sr_session* s, int step) {
@@ -277,13 +289,18 @@ int sm_count() {
 // iteration of set-up and, when split, half an iteration of merge.
 int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* order, int n) {
   const int forced = ss[0]->cfg.tail_split;
+  auto single_tail = [&](int r) {   // the query group's last block is a single tile
+    const int64_t rem = views[order[r]].lq % 256;
+    return rem > 0 && rem <= 128;
+  };
+  // Only when every query group ends in a single tile: in a batch that mixes
+  // them (the decoder's edge windows), parts of the few short last blocks
+  // cost more in per-CTA set-up than they save.
   int64_t min_kv = INT64_MAX;
   for (int r = 0; r < n; ++r) {
     const sr_session* s = ss[order[r]];
-    const ChunkView& view = views[order[r]];
-    const int64_t rem = view.lq % 256;
-    if (!s->buf.workspace || rem == 0 || rem > 128) return 1;   // no single-tile last block
-    min_kv = std::min(min_kv, key_tiles(s, view));
+    if (!single_tail(r) || !s->buf.workspace) return 1;
+    min_kv = std::min(min_kv, key_tiles(s, views[order[r]]));
   }
   const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, min_kv));
   if (forced > 0) return std::max(1, std::min(forced, cap));
@@ -359,9 +376,11 @@ sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, con
   const int split = st == SR_OK ? choose_tail_split(&s, &view, &order0, 1) : 1;
   s->buf.workspace = own;
   if (st != SR_OK) return st;
-  p.n_full_units = s->cfg.n_heads * (p.sess[0].nqb - 1);
+  int full = 0, tails = 0;
+  place_units(p.sess[0], s->cfg.n_heads, full, tails);
+  p.n_full_units = full;
   p.tail_split = split;
-  const int n_units = p.n_full_units + s->cfg.n_heads * split;
+  const int n_units = full + tails * split;
   p.n_sess = 1;
   p.n_heads = s->cfg.n_heads;
   p.scale_log2 = s->scale * 1.4426950408889634f;
@@ -583,13 +602,13 @@ static sr_status attention_view(sr_session* s, const ChunkView& view, int32_t st
   if (st == SR_OK) st = fill_session(p->sess[0], s, view, step, k, v, 0);
   int n_units = 0;
   if (st == SR_OK) {
-    // full 256-row blocks first (longest units), then the last block of every head
-    p->sess[0].unit_begin = 0;
-    p->sess[0].tail_begin = 0;
-    p->n_full_units = s->cfg.n_heads * (p->sess[0].nqb - 1);
+    // whole 256-row blocks first (longest units), then single-tile last blocks
+    int full = 0, tails = 0;
+    place_units(p->sess[0], s->cfg.n_heads, full, tails);
+    p->n_full_units = full;
     const int order0 = 0;
     p->tail_split = choose_tail_split(&s, &view, &order0, 1);
-    n_units = p->n_full_units + s->cfg.n_heads * p->tail_split;
+    n_units = full + tails * p->tail_split;
     p->n_sess = 1;
     p->n_heads = s->cfg.n_heads;
     p->scale_log2 = s->scale * 1.4426950408889634f;
@@ -684,15 +703,11 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
                                      {k_moving, v_moving, M}};
   const Segment prefix[sr::kSegs] = {{bk, bv, s->cfg.n_sink}, {nullptr, nullptr, 0}, {nullptr, nullptr, 0},
                                      {nullptr, nullptr, 0}};
-  int n = 0, full = 0;
+  int n = 0, full = 0, tails = 0;
   if (st == SR_OK) st = encode_group(p->sess[n++], moving, row_elems, P, M);
   if (st == SR_OK && P > 0) st = encode_group(p->sess[n++], prefix, row_elems, 0, P);
   if (st == SR_OK) {
-    for (int i = 0; i < n; ++i) {
-      p->sess[i].unit_begin = full;
-      p->sess[i].tail_begin = i * s->cfg.n_heads;
-      full += s->cfg.n_heads * (p->sess[i].nqb - 1);
-    }
+    for (int i = 0; i < n; ++i) place_units(p->sess[i], s->cfg.n_heads, full, tails);
     p->n_full_units = full;
     p->tail_split = 1;   // the groups share one session: no key-split workspace
     p->n_sess = n;
@@ -703,8 +718,7 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
     p->lse = lse;
     p->err_word = s->buf.err_word;
     p->timeout_ns = s->cfg.wait_timeout_ns;
-    cudaError_t e = sr::launch_attention_n(*p, s->cfg.head_dim, full + n * s->cfg.n_heads,
-                                           static_cast<cudaStream_t>(stream));
+    cudaError_t e = sr::launch_attention_n(*p, s->cfg.head_dim, full + tails, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) st = SR_ERR_CUDA;
   }
   delete p;
@@ -747,16 +761,13 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
   const int64_t row_elems = static_cast<int64_t>(s0->cfg.n_heads) * s0->cfg.head_dim;
   sr_status st = SR_OK;
   if (!encode_rows(&p->qmap, q, total, row_elems)) st = SR_ERR_CUDA;
-  // units: every session's full 256-row blocks (sessions by decreasing key
-  // count), then every session's last block -- longest work first
+  // units: every session's whole 256-row blocks (sessions by decreasing key
+  // count), then the single-tile last blocks -- longest work first
   int full = 0, tails = 0;
   for (int r = 0; st == SR_OK && r < n; ++r) {
     const int i = order[r];
     st = fill_session(p->sess[r], sessions[i], views[i], step, k, v, q_off[i]);
-    p->sess[r].unit_begin = full;
-    p->sess[r].tail_begin = tails;
-    full += s0->cfg.n_heads * (p->sess[r].nqb - 1);
-    tails += s0->cfg.n_heads;
+    if (st == SR_OK) place_units(p->sess[r], s0->cfg.n_heads, full, tails);
   }
   const int split = st == SR_OK ? choose_tail_split(sessions, views, order, n) : 1;
   const int units = full + tails * split;

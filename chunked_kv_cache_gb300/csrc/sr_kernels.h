@@ -46,7 +46,10 @@ struct alignas(128) AttnSession {
   int32_t q_row0;       // first row of this session in the packed q / o
   int32_t lq;           // query rows
   int32_t nqb;          // query blocks of 256 rows
-  int32_t unit_begin;   // first full-block unit of this session (full blocks come first)
+  int32_t nfull;        // blocks per head run as whole units: all of them, or all but a
+                        // single-tile (<= 128-row) last block
+  int32_t ntail;        // 1 when the last block is a single tile (run with the last-block units), else 0
+  int32_t unit_begin;   // first whole-block unit of this session (whole blocks come first)
   int32_t tail_begin;   // index of this session's last-block units among all last-block units
   float* ws_part;       // key-split partials: [H][kMaxTailSplit][128][d + 4] fp32 (NULL: no split)
   int32_t* ws_ctr;      // [H] per-head arrival counters (epoch << 4 | count)
