@@ -15,16 +15,20 @@
 // of a chunk may hold a single tile; then the two softmax groups take the two
 // halves of the key range of that one tile ("split" mode) and merge their
 // partial results at the end, so the tensor pipe still alternates between
-// two independent score tiles. Units run longest first: all full blocks, then
-// all last blocks.
+// two independent score tiles. Units run longest first: every whole block
+// (a last block of two tiles counts as whole), the blocks of one head side by
+// side so that they read its keys and values through L2, then the single-tile
+// last blocks. The kernel launches with programmatic stream serialization and
+// touches no global memory before griddepcontrol.wait.
 //
 // Warp roles:
 //   warps 0-3   softmax group 0 (thread i owns row i of its tile)
 //   warps 4-7   softmax group 1
 //   warp 8      MMA issuer (the whole warp in step, one elected lane issues):
 //               tcgen05.mma, accumulators in TMEM
-//   warp 9      TMA producer (one thread): Q once, then K/V tiles through an
-//               NSTAGE-deep shared-memory ring, in the order the MMA consumes
+//   warp 9      TMA producer (one thread): Q once, then K/V tiles in stage
+//               pairs (a K slot and a V slot behind one barrier), in the
+//               order the MMA consumes them
 //   warps 10-11 idle (they complete the third warpgroup)
 // Registers: launched at 168 per thread (384 x 168 = 64512); the third
 // warpgroup gives back down to 72 and the two softmax warpgroups take 216

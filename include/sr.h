@@ -18,7 +18,11 @@
  *   - Tensors are bf16, token-major [L][H][d], contiguous: row stride H*d elements.
  *     Every device pointer must be 16-byte aligned.
  *   - All calls are asynchronous on the given stream (a cudaStream_t passed as
- *     void*; NULL = the legacy default stream) and enqueue in call order.
+ *     void*; NULL = the legacy default stream) and enqueue in call order. The
+ *     RoPE/commit and attention kernels launch with programmatic stream
+ *     serialization: their CTAs may be scheduled while the previous kernel of
+ *     the stream drains, but they touch no global memory before it has
+ *     completed, so stream order holds for every buffer.
  *   - The library never allocates or frees device memory and never synchronises
  *     a stream: every device buffer is owned by the caller and must outlive the
  *     session; they are kept in the layout the attention kernel loads, so nothing
