@@ -10,7 +10,10 @@
 // caching"); cache slots that are still empty are simply not visited, so no
 // mask is needed (section 3.2 Iteration 3 item 4, the seqused_k idea).
 //
-// One CTA = one work unit = (session, head, block of 256 query rows). A full
+// A work unit = (session, head, block of 256 query rows). With a workspace
+// the launch is persistent: one CTA per SM takes units from a launch-wide
+// counter until none are left, and the producer loads the next unit's Q and
+// first K/V while the softmax groups finish the current one. A full
 // block is two 128-row tiles Q0, Q1 that share every K/V tile. The last block
 // of a chunk may hold a single tile; then the two softmax groups take the two
 // halves of the key range of that one tile ("split" mode) and merge their
@@ -31,8 +34,8 @@
 //               order the MMA consumes them
 //   warps 10-11 idle (they complete the third warpgroup)
 // Registers: launched at 168 per thread (384 x 168 = 64512); the third
-// warpgroup gives back down to 72 and the two softmax warpgroups take 216
-// each: 2 x 128 x 216 + 128 x 72 = 64512, the launch's total.
+// warpgroup gives back down to 136 and the two softmax warpgroups take 184
+// each: 2 x 128 x 184 + 128 x 136 = 64512, the launch's total.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) fp32 scores, O0 [256,256+d)
 // O1 [384,384+d) fp32 accumulators. P (bf16) is written back over the first
 // 64 columns of its S region and fed to the PV MMA straight from TMEM.
@@ -46,6 +49,8 @@
 // numerator and denominator consistent and avoids most rescales.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "sr_device.cuh"
 #include "sr_kernels.h"
 
@@ -58,8 +63,8 @@ constexpr int BN = 128;      // keys per K/V tile
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
 constexpr int kLaunchRegs = 168;
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsOther = 72;
+constexpr uint32_t kRegsSoftmax = 184;
+constexpr uint32_t kRegsOther = 136;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kAttnThreads * kLaunchRegs,
               "register split exceeds what the block is launched with");
 constexpr uint32_t kTmemCols = 512;
@@ -102,20 +107,39 @@ struct TileMap {
   }
 };
 
+constexpr int kUnitSlots = 4;   // units published ahead by the producer (ring of records)
+
+// One work unit as the producer decodes it; the MMA warp and the softmax
+// groups read the record after the barrier that publishes it.
+struct UnitRec {
+  int u;                 // unit index; -1 once the CTA has no more work
+  int si, head, part, parts;
+  int q_local0;          // first query row of the unit (session-local)
+  int n_qtiles;          // 2 (shared mode) or 1 (split mode)
+  int kv_lo, n_kv;       // the unit's range of the session's key tiles
+  TileMap tm;
+};
+
 struct SmemBars {
   uint64_t q_full;
-  uint64_t kv_full[8];    // up to kStagesSplit stages
+  uint64_t q_empty;       // the unit's QK MMAs are done: both Q slots may be reloaded
+  uint64_t kv_full[8];    // shared-mode pairs at [0, kPairs), split-mode pairs at [4, 4 + kPairsSplit)
   uint64_t kv_empty[8];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
+  uint64_t unit_ready[kUnitSlots];
+  uint64_t x_full;        // split mode: group 1 has published its running max and sum
+  uint64_t x_empty;       // split mode: group 0 has read them and both O accumulators
+  uint64_t part_done;     // key split: group 0's partial rows are published
+  uint64_t part_last;     // key split: `last` is set
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int last;       // key-split last block: this CTA is the last part and merges
   float xm[BM];   // split mode: group 1's running max / sum, handed to group 0
   float xl[BM];
-  TileMap tm;     // the unit's key tiles, read by the producer and the softmax groups
+  UnitRec rec[kUnitSlots];
 };
 
 // The key tiles each query tile walks, within the unit's range [lo, lo + n) of
@@ -160,28 +184,15 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
   }
 }
 
-template <int D, int NSESS>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams<NSESS> p) {
-  using C = Cfg<D>;
-  // The previous kernel of the stream may still be draining: the set-up below
-  // touches no global memory until grid_dep_wait(). The next kernel may be
-  // scheduled as soon as every CTA of this grid has started.
-  grid_dep_launch_dependents();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sKV = smem + C::kSmemQ;
-  SmemBars* bars = reinterpret_cast<SmemBars*>(smem + C::kSmemQ + C::kSmemKV);
-
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-
+// Decode unit u into its record: session, head, query block and key range,
+// and the tile map of its key segments (from the device frame counter for a
+// device-state call).
+template <int NSESS>
+__device__ __forceinline__ void make_unit(const AttnParams<NSESS>& p, int u, UnitRec& r) {
   int si, head, qb, part;
-  decode_unit(p, static_cast<int>(blockIdx.x), p.n_heads, si, head, qb, part);
+  decode_unit(p, u, p.n_heads, si, head, qb, part);
   const AttnSession& S = p.sess[si];
-  const int q_local0 = qb * 2 * BM;                       // first query row of the unit (session-local)
-  const int n_qtiles = min(2, (S.lq - q_local0 + BM - 1) / BM);
-  TileMap tl;   // registers only here; the loops read the shared-memory copy
+  TileMap tl;
 #pragma unroll
   for (int s = 0; s < kSegs; ++s) {
     tl.rows[s] = S.seg_rows[s];
@@ -190,7 +201,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   if (S.dev_n != nullptr) {
     // The visible ring frames follow the device frame counter: frames n-h ..
     // n-1 in slots (g mod W), one or two row ranges of the whole-ring maps.
-    grid_dep_wait();
     const int64_t n = *S.dev_n;
     const int W = S.ring_W, T = S.ring_T;
     const int v = static_cast<int>(min(n, static_cast<int64_t>(W)));
@@ -214,18 +224,70 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     tl.nt[s] = (tl.rows[s] + BN - 1) / BN;
     n_kv_all += tl.nt[s];
   }
+  r.si = si;
+  r.head = head;
+  r.part = part;
+  r.q_local0 = qb * 2 * BM;
+  r.n_qtiles = min(2, (S.lq - r.q_local0 + BM - 1) / BM);
   // a single-tile last block may be one of `parts` CTAs sharing its key range
-  const int parts = (n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
-  const int kv_lo = static_cast<int>(static_cast<int64_t>(part) * n_kv_all / parts);
-  const int n_kv = static_cast<int>(static_cast<int64_t>(part + 1) * n_kv_all / parts) - kv_lo;
-  const Walk wk{n_qtiles == 1, kv_lo, n_kv, n_qtiles == 1 ? (n_kv + 1) / 2 : n_kv};
+  r.parts = (r.n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
+  r.kv_lo = static_cast<int>(static_cast<int64_t>(part) * n_kv_all / r.parts);
+  r.n_kv = static_cast<int>(static_cast<int64_t>(part + 1) * n_kv_all / r.parts) - r.kv_lo;
+  r.tm = tl;
+  r.u = u;
+}
 
+__device__ __forceinline__ Walk unit_walk(const UnitRec& r) {
+  const bool split = r.n_qtiles == 1;
+  return Walk{split, r.kv_lo, r.n_kv, split ? (r.n_kv + 1) / 2 : r.n_kv};
+}
+
+// The unit a CTA takes after its first (which is its block index): the next
+// one of a launch-wide counter, or none when the launch runs one unit per
+// CTA. The counter holds (epoch << 32 | units taken); raising it to this
+// call's epoch first discards a count left by an earlier call that stopped
+// early. The last CTA to run out of units clears it (and the count of CTAs
+// that ran out), so that a replay of the same launch starts from zero.
+template <int NSESS>
+__device__ __forceinline__ int next_unit(const AttnParams<NSESS>& p) {
+  if (p.unit_ctr == nullptr) return p.n_units;
+  const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+  atomicMax(p.unit_ctr, tag);
+  const unsigned long long old = atomicAdd(p.unit_ctr, 1ull);
+  const int u = static_cast<int>(gridDim.x + (old & 0xffffffffull));
+  if (u >= p.n_units) {
+    atomicMax(p.unit_ctr + 1, tag);
+    const unsigned long long d = atomicAdd(p.unit_ctr + 1, 1ull);
+    if ((d & 0xffffffffull) == gridDim.x - 1) {
+      atomicExch(p.unit_ctr, 0ull);
+      atomicExch(p.unit_ctr + 1, 0ull);
+    }
+  }
+  return u;
+}
+
+template <int D, int NSESS>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams<NSESS> p) {
+  using C = Cfg<D>;
+  static_assert(sizeof(SmemBars) <= C::kSmemBar, "barrier area too small");
+  // The previous kernel of the stream may still be draining: the set-up below
+  // touches no global memory until grid_dep_wait(). The next kernel may be
+  // scheduled as soon as every CTA of this grid has started.
+  grid_dep_launch_dependents();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::kSmemQ;
+  SmemBars* bars = reinterpret_cast<SmemBars*>(smem + C::kSmemQ + C::kSmemKV);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
   WaitCtx wc{&bars->abort, p.err_word, p.timeout_ns};
 
   if (threadIdx.x == 0) {
-    bars->tm = tl;
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < C::kStagesSplit; ++s) {
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < 8; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
@@ -234,6 +296,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(&bars->p_full[t], BM);
       mbar_init(&bars->o_done[t], 1);
     }
+    for (int k = 0; k < kUnitSlots; ++k) mbar_init(&bars->unit_ready[k], 1);
+    mbar_init(&bars->x_full, BM);
+    mbar_init(&bars->x_empty, BM);
+    mbar_init(&bars->part_done, BM);
+    mbar_init(&bars->part_last, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -245,10 +312,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dep_wait();   // returns at once when it already returned above
+  grid_dep_wait();
   const uint32_t tmem = bars->tmem_base;
-  const TileMap& tm = bars->tm;
 
+  // Work: this CTA's first unit is its block index; a persistent launch (one
+  // CTA per SM) then takes further units from the launch-wide counter. Each
+  // role walks the same sequence of units: the producer decodes a unit into
+  // bars->rec[k % kUnitSlots] and publishes it on unit_ready (the softmax
+  // groups) and q_full (the MMA warp). Every barrier keeps running phase
+  // counts across units.
   if (warp >= 8) {
     regs_dec<kRegsOther>();
     if (warp == kTmaWarp && lane == 0) {
@@ -256,63 +328,115 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       tma_prefetch_map(&p.qmap);
-      for (int s = 0; s < kSegs; ++s)
-        if (tm.nt[s]) {
-          tma_prefetch_map(&S.kmap[s]);
-          tma_prefetch_map(&S.vmap[s]);
-        }
-      mbar_arrive_expect_tx(&bars->q_full, n_qtiles * C::kTileBytes);
-      for (int t = 0; t < n_qtiles; ++t)
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_2d(sQ + t * C::kTileBytes + a * C::kAtomBytes, &p.qmap, &bars->q_full,
-                      head * D + a * 64, S.q_row0 + q_local0 + t * BM, pol_q);
-      // K/V tiles travel in stage pairs behind one barrier: pair p is the
-      // slots 2p (a K tile) and 2p+1 (a V tile); the extra split-mode slot is
-      // the second Q slot.
-      const int npair = wk.split ? C::kPairsSplit : C::kPairs;
-      int q = 0;   // pair loads issued so far
       bool ok = true;
+      int uk = 0;            // units of this CTA so far
+      int u = blockIdx.x;
+      int q_last = -1;       // the last unit whose Q load was issued
+      int q_shared = 0, q_split = 0;   // pair loads issued so far, per mode
+      int mode = -1;         // the previous unit's mode
       auto slot_ptr = [&](int slot) -> uint8_t* {
         return slot < C::kStages ? sKV + slot * C::kTileBytes : sQ + C::kTileBytes;
       };
-      auto issue = [&](int j, bool is_v, int slot, uint64_t* bar) {
-        int seg, row0;
-        tm.locate(j, seg, row0);
-        const CUtensorMap* map = is_v ? &S.vmap[seg] : &S.kmap[seg];
-        uint8_t* dst = slot_ptr(slot);
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_2d(dst + a * C::kAtomBytes, map, bar, head * D + a * 64, tm.base[seg] + row0, pol_kv);
-      };
-      // one pair: key tile kj (if >= 0) and value tile vj (if >= 0)
-      auto load_pair = [&](int kj, int vj) {
-        if (!ok) return;
-        const int pr = q % npair;
-        if (q >= npair && !wait_bounded(&bars->kv_empty[pr], ((q / npair) - 1) & 1, wc, 1)) {
+      while (ok) {
+        // both Q slots (and the split-mode stage in the second) are free once
+        // the previous unit's MMAs that read them are done
+        if (uk > 0 && !wait_bounded(&bars->q_empty, (uk - 1) & 1, wc, 7)) {
           ok = false;
-          return;
+          break;
         }
-        mbar_arrive_expect_tx(&bars->kv_full[pr], ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
-        if (kj >= 0) issue(kj, false, 2 * pr, &bars->kv_full[pr]);
-        if (vj >= 0) issue(vj, true, 2 * pr + 1, &bars->kv_full[pr]);
-        ++q;
-      };
-      const int n_it = wk.iters();
-      if (!wk.split) {
-        // shared mode, iteration i: K_i (the S MMAs of both tiles) and V_{i-1}
-        for (int i = 0; i <= n_it && ok; ++i) load_pair(i < n_it ? i : -1, i > 0 ? i - 1 : -1);
-      } else {
-        // split mode, iteration i and tile t: K(t, i) and V(t, i-1), tile 0 first
-        for (int i = 0; i <= n_it && ok; ++i)
-          for (int t = 0; t < 2; ++t) {
-            const bool kq = i < wk.count(t), vq = i > 0 && i - 1 < wk.count(t);
-            if (kq || vq) load_pair(kq ? wk.kv(t, i) : -1, vq ? wk.kv(t, i - 1) : -1);
+        UnitRec& r = bars->rec[uk % kUnitSlots];
+        if (u >= p.n_units) {
+          r.u = -1;
+          mbar_arrive(&bars->unit_ready[uk % kUnitSlots]);
+          mbar_arrive(&bars->q_full);
+          break;
+        }
+        make_unit(p, u, r);
+        mbar_arrive(&bars->unit_ready[uk % kUnitSlots]);
+        const AttnSession& S = p.sess[r.si];
+        const TileMap& tm = r.tm;
+        const Walk wk = unit_walk(r);
+        const int md = wk.split ? 1 : 0;
+        // K/V travel in stage pairs behind one barrier: pair p is the slots
+        // 2p (a K tile) and 2p+1 (a V tile); the extra split-mode slot is the
+        // second Q slot. The two modes use separate barriers over the same
+        // slots, so on a change of mode the previous mode's pairs must have
+        // been released first.
+        if (mode >= 0 && mode != md) {
+          const int np = mode ? C::kPairsSplit : C::kPairs;
+          const int b0 = mode ? 4 : 0;
+          const int qm = mode ? q_split : q_shared;
+          for (int k = max(0, qm - np); k < qm && ok; ++k)
+            ok = wait_bounded(&bars->kv_empty[b0 + k % np], (k / np) & 1, wc, 1);
+          if (!ok) break;
+        }
+        mode = md;
+        for (int s = 0; s < kSegs; ++s)
+          if (tm.nt[s]) {
+            tma_prefetch_map(&S.kmap[s]);
+            tma_prefetch_map(&S.vmap[s]);
           }
+        mbar_arrive_expect_tx(&bars->q_full, r.n_qtiles * C::kTileBytes);
+        for (int t = 0; t < r.n_qtiles; ++t)
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_2d(sQ + t * C::kTileBytes + a * C::kAtomBytes, &p.qmap, &bars->q_full,
+                        r.head * D + a * 64, S.q_row0 + r.q_local0 + t * BM, pol_q);
+        q_last = uk;
+        const int npair = md ? C::kPairsSplit : C::kPairs;
+        const int bar0 = md ? 4 : 0;
+        int q = md ? q_split : q_shared;
+        auto issue = [&](int j, bool is_v, int slot, uint64_t* bar) {
+          int seg, row0;
+          tm.locate(j, seg, row0);
+          const CUtensorMap* map = is_v ? &S.vmap[seg] : &S.kmap[seg];
+          uint8_t* dst = slot_ptr(slot);
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_2d(dst + a * C::kAtomBytes, map, bar, r.head * D + a * 64, tm.base[seg] + row0, pol_kv);
+        };
+        // one pair: key tile kj (if >= 0) and value tile vj (if >= 0)
+        auto load_pair = [&](int kj, int vj) {
+          if (!ok) return;
+          const int pr = q % npair;
+          if (q >= npair && !wait_bounded(&bars->kv_empty[bar0 + pr], ((q / npair) - 1) & 1, wc, 1)) {
+            ok = false;
+            return;
+          }
+          uint64_t* bar = &bars->kv_full[bar0 + pr];
+          mbar_arrive_expect_tx(bar, ((kj >= 0 ? 1 : 0) + (vj >= 0 ? 1 : 0)) * C::kTileBytes);
+          if (kj >= 0) issue(kj, false, 2 * pr, bar);
+          if (vj >= 0) issue(vj, true, 2 * pr + 1, bar);
+          ++q;
+        };
+        const int n_it = wk.iters();
+        if (!wk.split) {
+          // shared mode, iteration i: K_i (the S MMAs of both tiles) and V_{i-1}
+          for (int i = 0; i <= n_it && ok; ++i) load_pair(i < n_it ? i : -1, i > 0 ? i - 1 : -1);
+        } else {
+          // split mode, iteration i and tile t: K(t, i) and V(t, i-1), tile 0 first
+          for (int i = 0; i <= n_it && ok; ++i)
+            for (int t = 0; t < 2; ++t) {
+              const bool kq = i < wk.count(t), vq = i > 0 && i - 1 < wk.count(t);
+              if (kq || vq) load_pair(kq ? wk.kv(t, i) : -1, vq ? wk.kv(t, i - 1) : -1);
+            }
+        }
+        if (md)
+          q_split = q;
+        else
+          q_shared = q;
+        if (!ok) break;
+        ++uk;
+        u = next_unit(p);   // taken late, once this unit's loads are all issued
       }
       if (!ok || bars->abort) {
         // let every copy this CTA started land before shared memory is released
-        wait_drain(&bars->q_full, 0, p.timeout_ns);
-        for (int k = max(0, q - npair); k < q; ++k)
-          wait_drain(&bars->kv_full[k % npair], (k / npair) & 1, p.timeout_ns);
+        if (q_last >= 0) wait_drain(&bars->q_full, q_last & 1, p.timeout_ns);
+        if (mode >= 0) {
+          const int np = mode ? C::kPairsSplit : C::kPairs;
+          const int b0 = mode ? 4 : 0;
+          const int qm = mode ? q_split : q_shared;
+          for (int k = max(0, qm - np); k < qm; ++k)
+            wait_drain(&bars->kv_full[b0 + k % np], (k / np) & 1, p.timeout_ns);
+        }
       }
     } else if (warp == kMmaWarp) {
       // ---------------------------------------------------------- MMA issuer
@@ -321,149 +445,177 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       // loop arithmetic run warp-uniform instead of as one divergent thread.
       const uint32_t leader = elect_one();
       bool issued_any = false;
-      bool ok = __all_sync(0xffffffffu, wait_bounded(&bars->q_full, 0, wc, 2));
+      bool ok = true;
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
-      // Position in the producer's sequence of stage pairs: pair and phase
-      // parity of the next one, advanced by counters (no division on this warp).
-      const int npair = wk.split ? C::kPairsSplit : C::kPairs;
-      int pc = 0;
-      uint32_t ph = 0;
-      auto take = [&]() -> int {   // wait for the next pair; returns its index
-        const int p0 = pc;
-        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->kv_full[p0], ph, wc, 3));
-        if (++pc == npair) {
-          pc = 0;
-          ph ^= 1u;
-        }
-        return p0;
-      };
-      auto wait_p = [&](int t, int it) {   // softmax group t has written P_t of iteration it
-        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->p_full[t], it & 1, wc, 4));
-        tc_fence_after();
-      };
+      int uk = 0;
+      // Position in the producer's sequence of stage pairs, per mode: pair and
+      // phase parity of the next one, advanced by counters (no division here).
+      int pc_shared = 0, pc_split = 0;
+      uint32_t ph_shared = 0, ph_split = 0;
+      uint32_t pb0 = 0, pb1 = 0;   // P tiles of each softmax group waited on so far
       // shared-memory address of a K/V stage (the extra split-mode stage is the second Q slot)
       auto stage_addr = [&](int stage) -> uint32_t {
         return stage < C::kStages ? skv + stage * C::kTileBytes : sq + C::kTileBytes;
       };
-      auto qk = [&](int t, int stage) {   // S_t = Q_t K^T
-        const uint32_t d_tmem = tmem + t * BN;
-        const uint32_t qt = sq + (wk.split ? 0 : t) * C::kTileBytes;
+      while (ok) {
+        ok = __all_sync(0xffffffffu, wait_bounded(&bars->q_full, uk & 1, wc, 2));
+        if (!ok) break;
+        const UnitRec& r = bars->rec[uk % kUnitSlots];
+        if (r.u < 0) break;
+        const Walk wk = unit_walk(r);
+        const int md = wk.split ? 1 : 0;
+        const int npair = md ? C::kPairsSplit : C::kPairs;
+        const int bar0 = md ? 4 : 0;
+        int pc = md ? pc_split : pc_shared;
+        uint32_t ph = md ? ph_split : ph_shared;
+        auto take = [&]() -> int {   // wait for the next pair; returns its index
+          const int p0 = pc;
+          if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->kv_full[bar0 + p0], ph, wc, 3));
+          if (++pc == npair) {
+            pc = 0;
+            ph ^= 1u;
+          }
+          return p0;
+        };
+        auto wait_p = [&](int t, int it) {   // softmax group t has written P_t of iteration it
+          const uint32_t par = ((t == 0 ? pb0 : pb1) + static_cast<uint32_t>(it)) & 1u;
+          if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->p_full[t], par, wc, 4));
+          tc_fence_after();
+        };
+        auto qk = [&](int t, int stage) {   // S_t = Q_t K^T
+          const uint32_t d_tmem = tmem + t * BN;
+          const uint32_t qt = sq + (wk.split ? 0 : t) * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kAtomBytes + (kk % 4) * 32;
-          const uint64_t ad = sdesc_sw128(qt + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(stage_addr(stage) + off, 16, 1024);
-          mma_ss_w(d_tmem, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u, leader);
-        }
-      };
-      auto pv = [&](int t, int stage, bool acc) {   // O_t += P_t V
-        const uint32_t d_tmem = tmem + 256 + t * 128;
-        const uint32_t a_tmem = tmem + t * BN;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kAtomBytes + (kk % 4) * 32;
+            const uint64_t ad = sdesc_sw128(qt + off, 16, 1024);
+            const uint64_t bd = sdesc_sw128(stage_addr(stage) + off, 16, 1024);
+            mma_ss_w(d_tmem, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u, leader);
+          }
+        };
+        auto pv = [&](int t, int stage, bool acc) {   // O_t += P_t V
+          const uint32_t d_tmem = tmem + 256 + t * 128;
+          const uint32_t a_tmem = tmem + t * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(stage_addr(stage) + kk * 16 * 128, C::kAtomBytes, 1024);
-          mma_ts_w(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u, leader);
-        }
-      };
-      if (!wk.split) {
-        // Shared mode: both tiles walk all n key tiles, and the loop carries
-        // nothing between two MMA bursts but the waits it cannot avoid. The
-        // tensor pipe queues only a few MMAs, so every cycle of other work
-        // between bursts (a division, a loop back edge, a branch) is a cycle
-        // the pipe may stand idle: stages advance by counters and the first
-        // and last iterations are peeled off, so the body branches only to
-        // leave on an abort.
-        const int n = wk.n;
-        // iteration 0: S_0 of both tiles (pair 0 holds K_0 only)
-        const int p0 = take();
-        if (ok) {
-          tc_fence_after();
-          qk(0, 2 * p0);
-          tc_commit_w(&bars->s_full[0], leader);
-          qk(1, 2 * p0);
-          tc_commit_w(&bars->s_full[1], leader);
-          tc_commit_w(&bars->kv_empty[p0], leader);
-          issued_any = true;
-        }
-        // iterations 1 .. n-1: PV_{i-1} and S_i of both tiles from one pair
-        // (K_i, V_{i-1}). Its wait comes first, while the warp would otherwise
-        // be waiting for softmax group 0; between S0_i and PV1_{i-1} there is
-        // only that group's wait.
-        for (int i = 1; i < n && ok; ++i) {
-          const int pi = take();
-          tc_fence_after();
-          wait_p(0, i - 1);
-          if (!ok) break;
-          pv(0, 2 * pi + 1, i > 1);
-          qk(0, 2 * pi);
-          tc_commit_w(&bars->s_full[0], leader);
-          wait_p(1, i - 1);
-          if (!ok) break;
-          pv(1, 2 * pi + 1, i > 1);
-          qk(1, 2 * pi);
-          tc_commit_w(&bars->s_full[1], leader);
-          tc_commit_w(&bars->kv_empty[pi], leader);
-        }
-        // last: PV_{n-1} of both tiles (the last pair holds V_{n-1} only)
-        if (ok) {
-          const int pl = take();
-          tc_fence_after();
-          wait_p(0, n - 1);
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bd = sdesc_sw128(stage_addr(stage) + kk * 16 * 128, C::kAtomBytes, 1024);
+            mma_ts_w(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u, leader);
+          }
+        };
+        if (!wk.split) {
+          // Shared mode: both tiles walk all n key tiles, and the loop carries
+          // nothing between two MMA bursts but the waits it cannot avoid. The
+          // tensor pipe queues only a few MMAs, so every cycle of other work
+          // between bursts (a division, a loop back edge, a branch) is a cycle
+          // the pipe may stand idle: stages advance by counters and the first
+          // and last iterations are peeled off, so the body branches only to
+          // leave on an abort.
+          const int n = wk.n;
+          // iteration 0: S_0 of both tiles (pair 0 holds K_0 only)
+          const int p0 = take();
           if (ok) {
-            pv(0, 2 * pl + 1, n > 1);
-            tc_commit_w(&bars->o_done[0], leader);
-            wait_p(1, n - 1);
+            tc_fence_after();
+            qk(0, 2 * p0);
+            tc_commit_w(&bars->s_full[0], leader);
+            qk(1, 2 * p0);
+            tc_commit_w(&bars->s_full[1], leader);
+            tc_commit_w(&bars->kv_empty[bar0 + p0], leader);
+            issued_any = true;
           }
+          // iterations 1 .. n-1: PV_{i-1} and S_i of both tiles from one pair
+          // (K_i, V_{i-1}). Its wait comes first, while the warp would otherwise
+          // be waiting for softmax group 0; between S0_i and PV1_{i-1} there is
+          // only that group's wait.
+          for (int i = 1; i < n && ok; ++i) {
+            const int pi = take();
+            tc_fence_after();
+            wait_p(0, i - 1);
+            if (!ok) break;
+            pv(0, 2 * pi + 1, i > 1);
+            qk(0, 2 * pi);
+            tc_commit_w(&bars->s_full[0], leader);
+            wait_p(1, i - 1);
+            if (!ok) break;
+            pv(1, 2 * pi + 1, i > 1);
+            qk(1, 2 * pi);
+            tc_commit_w(&bars->s_full[1], leader);
+            tc_commit_w(&bars->kv_empty[bar0 + pi], leader);
+          }
+          // every S MMA of the unit is issued: the Q slots free up as they finish
+          if (ok) tc_commit_w(&bars->q_empty, leader);
+          // last: PV_{n-1} of both tiles (the last pair holds V_{n-1} only)
           if (ok) {
-            pv(1, 2 * pl + 1, n > 1);
-            tc_commit_w(&bars->o_done[1], leader);
-            tc_commit_w(&bars->kv_empty[pl], leader);
-          }
-        }
-      } else {
-        // Split mode (a single-tile last block): tile 0 walks c0 key tiles,
-        // tile 1 the next c1 (c0 - c1 is 0 or 1). Iteration i takes, per tile
-        // t, one pair holding K(t, i) and V(t, i-1); tile 1's wait comes after
-        // tile 0's MMAs are queued.
-        const int c0 = wk.count(0), c1 = wk.count(1);
-        for (int i = 0; i <= c0 && ok; ++i) {
-          const bool p0 = i > 0 && i - 1 < c0, q0 = i < c0;
-          if (p0 || q0) {
-            const int pr = take();   // K(0, i) and V(0, i-1)
-            if (!ok) break;
+            const int pl = take();
             tc_fence_after();
-            if (p0) {
-              wait_p(0, i - 1);
-              if (!ok) break;
-              pv(0, 2 * pr + 1, i > 1);
-              if (i == c0) tc_commit_w(&bars->o_done[0], leader);
+            wait_p(0, n - 1);
+            if (ok) {
+              pv(0, 2 * pl + 1, n > 1);
+              tc_commit_w(&bars->o_done[0], leader);
+              wait_p(1, n - 1);
             }
-            if (q0) {
-              qk(0, 2 * pr);
-              tc_commit_w(&bars->s_full[0], leader);
-              issued_any = true;
+            if (ok) {
+              pv(1, 2 * pl + 1, n > 1);
+              tc_commit_w(&bars->o_done[1], leader);
+              tc_commit_w(&bars->kv_empty[bar0 + pl], leader);
             }
-            tc_commit_w(&bars->kv_empty[pr], leader);
           }
-          const bool p1 = i > 0 && i - 1 < c1, q1 = i < c1;
-          if (p1 || q1) {
-            const int pr = take();   // K(1, i) and V(1, i-1)
-            if (!ok) break;
-            tc_fence_after();
-            if (p1) {
-              wait_p(1, i - 1);
+        } else {
+          // Split mode (a single-tile last block): tile 0 walks c0 key tiles,
+          // tile 1 the next c1 (c0 - c1 is 0 or 1). Iteration i takes, per tile
+          // t, one pair holding K(t, i) and V(t, i-1); tile 1's wait comes after
+          // tile 0's MMAs are queued.
+          const int c0 = wk.count(0), c1 = wk.count(1);
+          for (int i = 0; i <= c0 && ok; ++i) {
+            const bool p0 = i > 0 && i - 1 < c0, q0 = i < c0;
+            if (p0 || q0) {
+              const int pr = take();   // K(0, i) and V(0, i-1)
               if (!ok) break;
-              pv(1, 2 * pr + 1, i > 1);
-              if (i == c1) tc_commit_w(&bars->o_done[1], leader);
+              tc_fence_after();
+              if (p0) {
+                wait_p(0, i - 1);
+                if (!ok) break;
+                pv(0, 2 * pr + 1, i > 1);
+                if (i == c0) tc_commit_w(&bars->o_done[0], leader);
+              }
+              if (q0) {
+                qk(0, 2 * pr);
+                tc_commit_w(&bars->s_full[0], leader);
+                issued_any = true;
+              }
+              tc_commit_w(&bars->kv_empty[bar0 + pr], leader);
             }
-            if (q1) {
-              qk(1, 2 * pr);
-              tc_commit_w(&bars->s_full[1], leader);
+            const bool p1 = i > 0 && i - 1 < c1, q1 = i < c1;
+            if (p1 || q1) {
+              const int pr = take();   // K(1, i) and V(1, i-1)
+              if (!ok) break;
+              tc_fence_after();
+              if (p1) {
+                wait_p(1, i - 1);
+                if (!ok) break;
+                pv(1, 2 * pr + 1, i > 1);
+                if (i == c1) tc_commit_w(&bars->o_done[1], leader);
+              }
+              if (q1) {
+                qk(1, 2 * pr);
+                tc_commit_w(&bars->s_full[1], leader);
+              }
+              tc_commit_w(&bars->kv_empty[bar0 + pr], leader);
             }
-            tc_commit_w(&bars->kv_empty[pr], leader);
           }
+          // the second Q slot served as a K/V stage: free once every MMA is done
+          if (ok) tc_commit_w(&bars->q_empty, leader);
         }
+        if (md) {
+          pc_split = pc;
+          ph_split = ph;
+        } else {
+          pc_shared = pc;
+          ph_shared = ph;
+        }
+        pb0 += static_cast<uint32_t>(wk.count(0));
+        pb1 += static_cast<uint32_t>(wk.count(1));
+        ++uk;
       }
       if (!ok && issued_any) {
         // no tensor-core work may still be running when TMEM is released
@@ -481,226 +633,257 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     const uint32_t t_o = tmem + lane_base + 256 + t * 128;
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
-    float m = -INFINITY;   // running max of scaled scores, log2 units
-    float l = 0.f;         // running sum of exp2(score - m)
-    const int cnt = wk.count(t);
     bool ok = true;
-    for (int j = 0; ok && j < cnt; ++j) {
-      // ragged tail of a segment: keys past its end are not part of the window.
-      // Looked up before the wait, so the shared-memory latency hides behind it.
-      int seg, row0;
-      tm.locate(wk.kv(t, j), seg, row0);
-      const int valid = tm.rows[seg] - row0;
-      ok = wait_bounded(&bars->s_full[t], j & 1, wc, 5);
-      ok = __all_sync(0xffffffffu, ok);
+    int uk = 0;
+    uint32_t sb = 0;             // S tiles of this group consumed so far
+    uint32_t od0 = 0, od1 = 0;   // o_done completions of each tile so far
+    uint32_t nx = 0;             // split-mode units so far
+    uint32_t nk = 0;             // key-split units so far
+    while (ok) {
+      ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[uk % kUnitSlots], (uk / kUnitSlots) & 1, wc, 8));
       if (!ok) break;
-      tc_fence_after();
-      uint32_t r[4][32];
+      const UnitRec& r = bars->rec[uk % kUnitSlots];
+      if (r.u < 0) break;
+      const Walk wk = unit_walk(r);
+      const TileMap& tm = r.tm;
+      const AttnSession& S = p.sess[r.si];
+      const int head = r.head, part = r.part, parts = r.parts;
+      float m = -INFINITY;   // running max of scaled scores, log2 units
+      float l = 0.f;         // running sum of exp2(score - m)
+      const int cnt = wk.count(t);
+      for (int j = 0; ok && j < cnt; ++j) {
+        // ragged tail of a segment: keys past its end are not part of the window.
+        // Looked up before the wait, so the shared-memory latency hides behind it.
+        int seg, row0;
+        tm.locate(wk.kv(t, j), seg, row0);
+        const int valid = tm.rows[seg] - row0;
+        ok = wait_bounded(&bars->s_full[t], (sb + static_cast<uint32_t>(j)) & 1u, wc, 5);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t rr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, r[c]);
-      tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, rr[c]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_fix(r[c]);
-      float* s = reinterpret_cast<float*>(&r[0][0]);
-      if (valid < BN) {
+        for (int c = 0; c < 4; ++c) tmem_fix(rr[c]);
+        float* s = reinterpret_cast<float*>(&rr[0][0]);
+        if (valid < BN) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i)
-          if (i >= valid) s[i] = -INFINITY;
-      }
-      float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]), a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
-#pragma unroll
-      for (int i = 8; i < BN; i += 8) {
-        a0 = fmax3(a0, s[i], s[i + 1]);
-        a1 = fmax3(a1, s[i + 2], s[i + 3]);
-        a2 = fmax3(a2, s[i + 4], s[i + 5]);
-        a3 = fmax3(a3, s[i + 6], s[i + 7]);
-      }
-      const float mt = fmax3(a0, a1, fmaxf(a2, a3)) * sl2;
-      const bool need = (j == 0) || (mt > m + kRescaleThreshold);
-      float f = 1.f;                    // factor that takes O and l to the new maximum
-      const bool rescale = __any_sync(0xffffffffu, need);
-      if (rescale) {
-        const float m_new = fmaxf(m, mt);
-        if (j > 0) f = ex2_approx(m - m_new);
-        m = m_new;
-      }
-      const float2 negm = make_float2(-m, -m);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int i = c * 32 + 2 * k;
-          const float2 x = __ffma2_rn(make_float2(s[i], s[i + 1]), sl2x2, negm);
-          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[k % 4] = __fadd2_rn(acc[k % 4], e);
-          pk[k] = pack_bf16x2(e.x, e.y);
+          for (int i = 0; i < BN; ++i)
+            if (i >= valid) s[i] = -INFINITY;
         }
-        tmem_st16(t_s + c * 16, pk);
+        float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]), a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
+#pragma unroll
+        for (int i = 8; i < BN; i += 8) {
+          a0 = fmax3(a0, s[i], s[i + 1]);
+          a1 = fmax3(a1, s[i + 2], s[i + 3]);
+          a2 = fmax3(a2, s[i + 4], s[i + 5]);
+          a3 = fmax3(a3, s[i + 6], s[i + 7]);
+        }
+        const float mt = fmax3(a0, a1, fmaxf(a2, a3)) * sl2;
+        const bool need = (j == 0) || (mt > m + kRescaleThreshold);
+        float f = 1.f;                    // factor that takes O and l to the new maximum
+        const bool rescale = __any_sync(0xffffffffu, need);
+        if (rescale) {
+          const float m_new = fmaxf(m, mt);
+          if (j > 0) f = ex2_approx(m - m_new);
+          m = m_new;
+        }
+        const float2 negm = make_float2(-m, -m);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i = c * 32 + 2 * k;
+            const float2 x = __ffma2_rn(make_float2(s[i], s[i + 1]), sl2x2, negm);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            acc[k % 4] = __fadd2_rn(acc[k % 4], e);
+            pk[k] = pack_bf16x2(e.x, e.y);
+          }
+          tmem_st16(t_s + c * 16, pk);
+        }
+        const float2 s01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        l = l * f + (s01.x + s01.y);
+        if (rescale && j > 0) {
+          // O was last written by PV_{j-1}, which completed before S_j was
+          // signalled (in-order tensor pipe; a commit covers all prior MMAs);
+          // PV_j is not issued before this thread arrives on p_full below.
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+            tmem_fix(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(t_o + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
       }
-      const float2 s01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-      l = l * f + (s01.x + s01.y);
-      if (rescale && j > 0) {
-        // O was last written by PV_{j-1}, which completed before S_j was
-        // signalled (in-order tensor pipe; a commit covers all prior MMAs);
-        // PV_j is not issued before this thread arrives on p_full below.
+      sb += static_cast<uint32_t>(cnt);
+
+      // ---- epilogue: normalise and store (in split mode group 0 merges both halves)
+      const int q_local = r.q_local0 + (wk.split ? 0 : t) * BM + row;
+      const bool live = q_local < S.lq;
+      const int64_t out_row = static_cast<int64_t>(S.q_row0) + q_local;
+      const bool merge = wk.split && wk.count(1) > 0;
+      const uint32_t w0 = od0, w1 = od1;   // this unit's o_done phases
+      od0 += 1u;
+      od1 += (!wk.split || wk.count(1) > 0) ? 1u : 0u;
+      if (wk.split && t == 1) {
+        // hand (m, l) to group 0, then wait until it has read them and O_1:
+        // this group's next P (and so the next PV into O_1) comes only after
+        bars->xm[row] = (ok && cnt > 0) ? m : -INFINITY;
+        bars->xl[row] = (ok && cnt > 0) ? l : 0.f;
+        mbar_arrive(&bars->x_full);
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->x_empty, nx & 1u, wc, 9));
+        ++nx;
+        ++uk;
+        continue;
+      }
+      if (wk.split && ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->x_full, nx & 1u, wc, 9));
+      if (ok) {
+        ok = wait_bounded(&bars->o_done[t], (t == 0 ? w0 : w1) & 1u, wc, 6);
+        if (ok && merge) ok = wait_bounded(&bars->o_done[1], w1 & 1u, wc, 6);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      // one part of a key-split last block publishes fp32 rows and their log2-sum-exp
+      float* pdst = parts > 1 ? S.ws_part + ((static_cast<int64_t>(head) * kMaxTailSplit + part) * BM + row) * (D + 4)
+                              : nullptr;
+      if (ok) {
+        tc_fence_after();
+        float f0 = 1.f, f1 = 0.f;
+        if (merge) {
+          const float m1 = bars->xm[row], l1 = bars->xl[row];
+          const float mm = fmaxf(m, m1);
+          f0 = ex2_approx(m - mm);
+          f1 = ex2_approx(m1 - mm);
+          l = l * f0 + l1 * f1;
+          m = mm;
+        }
+        const float inv_l = 1.f / l;
+        f0 *= inv_l;
+        f1 *= inv_l;
+        __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
+        const uint32_t t_o1 = tmem + lane_base + 256 + 128;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(t_o + c * 32, o);
           tmem_wait_ld();
           tmem_fix(o);
+          if (merge) {
+            uint32_t o1[32];
+            tmem_ld32(t_o1 + c * 32, o1);
+            tmem_wait_ld();
+            tmem_fix(o1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(t_o + c * 32, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
-    }
-
-    // ---- epilogue: normalise and store (in split mode group 0 merges both halves)
-    const int q_local = q_local0 + (wk.split ? 0 : t) * BM + row;
-    const bool live = q_local < S.lq;
-    const int64_t out_row = static_cast<int64_t>(S.q_row0) + q_local;
-    bool merge = false;
-    if (wk.split) {
-      if (t == 1) {
-        bars->xm[row] = (ok && cnt > 0) ? m : -INFINITY;
-        bars->xl[row] = (ok && cnt > 0) ? l : 0.f;
-      }
-      named_sync(1, 2 * 4 * 32);
-      merge = wk.count(1) > 0;
-    }
-    const bool writer = !wk.split || t == 0;
-    if (writer && ok) {
-      ok = wait_bounded(&bars->o_done[t], 0, wc, 6);
-      if (ok && merge) ok = wait_bounded(&bars->o_done[1], 0, wc, 6);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (writer && ok) {
-      tc_fence_after();
-      float f0 = 1.f, f1 = 0.f;
-      if (merge) {
-        const float m1 = bars->xm[row], l1 = bars->xl[row];
-        const float mm = fmaxf(m, m1);
-        f0 = ex2_approx(m - mm);
-        f1 = ex2_approx(m1 - mm);
-        l = l * f0 + l1 * f1;
-        m = mm;
-      }
-      const float inv_l = 1.f / l;
-      f0 *= inv_l;
-      f1 *= inv_l;
-      __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
-      // one part of a key-split last block publishes fp32 rows and their log2-sum-exp
-      float* pdst = parts > 1 ? S.ws_part + ((static_cast<int64_t>(head) * kMaxTailSplit + part) * BM + row) * (D + 4)
-                              : nullptr;
-      const uint32_t t_o1 = tmem + lane_base + 256 + 128;
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * f0 + __uint_as_float(o1[i]) * f1);
+          } else {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c * 32, o);
-        tmem_wait_ld();
-        tmem_fix(o);
-        if (merge) {
-          uint32_t o1[32];
-          tmem_ld32(t_o1 + c * 32, o1);
-          tmem_wait_ld();
-          tmem_fix(o1);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f0);
+          }
+          if (live) {
+            if (pdst) {
+              float4* d4 = reinterpret_cast<float4*>(pdst + c * 32);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            o[i] = __float_as_uint(__uint_as_float(o[i]) * f0 + __uint_as_float(o1[i]) * f1);
-        } else {
+              for (int i = 0; i < 8; ++i)
+                d4[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                    __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+            } else {
+              uint4 pkt[4];
+              uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f0);
+              for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = pkt[i];
+            }
+          }
         }
         if (live) {
-          if (pdst) {
-            float4* d4 = reinterpret_cast<float4*>(pdst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                  __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
-          } else {
-            uint4 pkt[4];
-            uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = pkt[i];
-          }
+          const float lse2 = m + __log2f(l);
+          if (pdst)
+            pdst[D] = lse2;
+          else if (p.lse != nullptr)
+            p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = lse2 * 0.69314718055994531f;
         }
       }
-      if (live) {
-        const float lse2 = m + __log2f(l);
-        if (pdst)
-          pdst[D] = lse2;
-        else if (p.lse != nullptr)
-          p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = lse2 * 0.69314718055994531f;
+      // group 1 may go on: its (m, l) and O_1 have been read
+      if (wk.split) {
+        tc_fence_before();
+        mbar_arrive(&bars->x_empty);
+        ++nx;
       }
-    }
-    if (writer && parts > 1) {
-      // Every part has published its rows; the last part to arrive merges them.
-      // The counter holds (epoch << 4 | arrivals): raising it to this call's
-      // epoch first discards any count left by an earlier, aborted call. The
-      // last part clears it once every part has arrived, so that a replay of
-      // the same launch (a CUDA graph repeats the epoch) starts from zero.
-      __threadfence();
-      named_sync(2, BM);
-      if (threadIdx.x == 0) {
-        int last = 0;
-        if (ok) {
-          int* ctr = S.ws_ctr + head;
-          atomicMax(ctr, S.epoch << 4);
-          const int old = atomicAdd(ctr, 1);
-          last = ((old >> 4) == S.epoch) && ((old & 15) == parts - 1);
-          if (last) atomicExch(ctr, 0);
-        }
-        bars->last = last;
-      }
-      named_sync(2, BM);
-      if (bars->last && live) {
+      if (parts > 1) {
+        // Every part has published its rows; the last part to arrive merges them.
+        // The counter holds (epoch << 4 | arrivals): raising it to this call's
+        // epoch first discards any count left by an earlier, aborted call. The
+        // last part clears it once every part has arrived, so that a replay of
+        // the same launch (a CUDA graph repeats the epoch) starts from zero.
         __threadfence();
-        const float* base = S.ws_part + (static_cast<int64_t>(head) * kMaxTailSplit * BM + row) * (D + 4);
-        const int64_t pstride = static_cast<int64_t>(BM) * (D + 4);
-        float w[kMaxTailSplit];
-        float mx = -INFINITY;
-        for (int k = 0; k < parts; ++k) {
-          w[k] = __ldcg(base + k * pstride + D);
-          mx = fmaxf(mx, w[k]);
-        }
-        float L = 0.f;
-        for (int k = 0; k < parts; ++k) {
-          w[k] = ex2_approx(w[k] - mx);
-          L += w[k];
-        }
-        const float invL = 1.f / L;
-        for (int k = 0; k < parts; ++k) w[k] *= invL;
-        __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 8) {
-          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int k = 0; k < parts; ++k) {
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c));
-            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c + 4));
-            a[0] += w[k] * x0.x; a[1] += w[k] * x0.y; a[2] += w[k] * x0.z; a[3] += w[k] * x0.w;
-            a[4] += w[k] * x1.x; a[5] += w[k] * x1.y; a[6] += w[k] * x1.z; a[7] += w[k] * x1.w;
+        mbar_arrive(&bars->part_done);
+        if (threadIdx.x == 0) {
+          int last = 0;
+          if (ok && wait_bounded(&bars->part_done, nk & 1u, wc, 10)) {
+            int* ctr = S.ws_ctr + head;
+            atomicMax(ctr, S.epoch << 4);
+            const int old = atomicAdd(ctr, 1);
+            last = ((old >> 4) == S.epoch) && ((old & 15) == parts - 1);
+            if (last) atomicExch(ctr, 0);
           }
-          uint4 pkt;
-          pkt.x = pack_bf16x2(a[0], a[1]);
-          pkt.y = pack_bf16x2(a[2], a[3]);
-          pkt.z = pack_bf16x2(a[4], a[5]);
-          pkt.w = pack_bf16x2(a[6], a[7]);
-          *reinterpret_cast<uint4*>(dst + c) = pkt;
+          bars->last = last;
+          mbar_arrive(&bars->part_last);
         }
-        if (p.lse != nullptr)
-          p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = (mx + __log2f(L)) * 0.69314718055994531f;
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->part_last, nk & 1u, wc, 10));
+        ++nk;
+        if (ok && bars->last && live) {
+          __threadfence();
+          const float* base = S.ws_part + (static_cast<int64_t>(head) * kMaxTailSplit * BM + row) * (D + 4);
+          const int64_t pstride = static_cast<int64_t>(BM) * (D + 4);
+          float w[kMaxTailSplit];
+          float mx = -INFINITY;
+          for (int k = 0; k < parts; ++k) {
+            w[k] = __ldcg(base + k * pstride + D);
+            mx = fmaxf(mx, w[k]);
+          }
+          float L = 0.f;
+          for (int k = 0; k < parts; ++k) {
+            w[k] = ex2_approx(w[k] - mx);
+            L += w[k];
+          }
+          const float invL = 1.f / L;
+          for (int k = 0; k < parts; ++k) w[k] *= invL;
+          __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
+#pragma unroll 1
+          for (int c = 0; c < D; c += 8) {
+            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < parts; ++k) {
+              const float4 x0 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c));
+              const float4 x1 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c + 4));
+              a[0] += w[k] * x0.x; a[1] += w[k] * x0.y; a[2] += w[k] * x0.z; a[3] += w[k] * x0.w;
+              a[4] += w[k] * x1.x; a[5] += w[k] * x1.y; a[6] += w[k] * x1.z; a[7] += w[k] * x1.w;
+            }
+            uint4 pkt;
+            pkt.x = pack_bf16x2(a[0], a[1]);
+            pkt.y = pack_bf16x2(a[2], a[3]);
+            pkt.z = pack_bf16x2(a[4], a[5]);
+            pkt.w = pack_bf16x2(a[6], a[7]);
+            *reinterpret_cast<uint4*>(dst + c) = pkt;
+          }
+          if (p.lse != nullptr)
+            p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = (mx + __log2f(L)) * 0.69314718055994531f;
+        }
       }
+      ++uk;
     }
   }
 
@@ -734,18 +917,27 @@ cudaError_t attn_prepare(int head_dim, int nsess_template) {
   return nsess_template == 1 ? set_attr<64, 1>() : set_attr<64, kAttnMaxBatch>();
 }
 
-cudaError_t launch_attention_1(const AttnParams<1>& p, int head_dim, int n_units, cudaStream_t st) {
-  if (n_units == 0) return cudaSuccess;
+namespace {
+template <int NSESS>
+unsigned attn_grid(const AttnParams<NSESS>& p) {
+  const int n = p.n_units;
+  return static_cast<unsigned>(p.unit_ctr != nullptr ? std::min(n, sm_count()) : n);
+}
+}  // namespace
+
+cudaError_t launch_attention_1(const AttnParams<1>& p, int head_dim, cudaStream_t st) {
+  if (p.n_units <= 0) return cudaSuccess;
   if (head_dim == 128)
-    return launch_dependent(attn_kernel<128, 1>, n_units, kAttnThreads, Cfg<128>::kSmemBytes, st, p);
-  return launch_dependent(attn_kernel<64, 1>, n_units, kAttnThreads, Cfg<64>::kSmemBytes, st, p);
+    return launch_dependent(attn_kernel<128, 1>, attn_grid(p), kAttnThreads, Cfg<128>::kSmemBytes, st, p);
+  return launch_dependent(attn_kernel<64, 1>, attn_grid(p), kAttnThreads, Cfg<64>::kSmemBytes, st, p);
 }
 
-cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim, int n_units, cudaStream_t st) {
-  if (n_units == 0) return cudaSuccess;
+cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim, cudaStream_t st) {
+  if (p.n_units <= 0) return cudaSuccess;
   if (head_dim == 128)
-    return launch_dependent(attn_kernel<128, kAttnMaxBatch>, n_units, kAttnThreads, Cfg<128>::kSmemBytes, st, p);
-  return launch_dependent(attn_kernel<64, kAttnMaxBatch>, n_units, kAttnThreads, Cfg<64>::kSmemBytes, st, p);
+    return launch_dependent(attn_kernel<128, kAttnMaxBatch>, attn_grid(p), kAttnThreads, Cfg<128>::kSmemBytes, st,
+                            p);
+  return launch_dependent(attn_kernel<64, kAttnMaxBatch>, attn_grid(p), kAttnThreads, Cfg<64>::kSmemBytes, st, p);
 }
 
 // ---------------------------------------------------------------- diagnostics

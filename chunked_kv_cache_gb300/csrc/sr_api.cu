@@ -212,6 +212,20 @@ void place_units(sr::AttnSession& g, int n_heads, int& full, int& tails) {
   tails += n_heads * g.ntail;
 }
 
+// The launch's unit count, and the unit counter of a persistent launch: it
+// lives at the start of the first group's workspace (none: one unit per CTA).
+template <int N>
+void set_units(sr::AttnParams<N>& p, int n_units, const sr_session* first) {
+  p.n_units = n_units;
+  if (first->buf.workspace != nullptr && p.sess[0].ws_ctr != nullptr) {
+    p.unit_ctr = static_cast<unsigned long long*>(first->buf.workspace);
+    p.epoch = p.sess[0].epoch;
+  } else {
+    p.unit_ctr = nullptr;
+    p.epoch = 0;
+  }
+}
+
 const char* bank_ptr(const void* bank, const sr_session* s, int step) {
   const size_t row_bytes = static_cast<size_t>(s->cfg.n_heads) * s->cfg.head_dim * 2;
   return static_cast<const char*>(bank) + static_cast<size_t>(step) * s->cfg.n_sink * row_bytes;
@@ -247,7 +261,7 @@ sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& vie
   }
   if (s->buf.workspace) {
     char* ws = static_cast<char*>(s->buf.workspace);
-    out.ws_ctr = reinterpret_cast<int32_t*>(ws);
+    out.ws_ctr = reinterpret_cast<int32_t*>(ws + sr::kWsUnitCtrBytes);
     out.ws_part = reinterpret_cast<float*>(ws + sr::ws_counter_bytes(s->cfg.n_heads));
     s->epoch = (s->epoch + 1) & 0x07FFFFFF;
     if (s->epoch == 0) s->epoch = 1;
@@ -265,18 +279,6 @@ int64_t key_tiles(const sr_session* s, const ChunkView& view) {
   int64_t n = 0;
   for (int64_t r : rows) n += (r + 127) / 128;
   return n;
-}
-
-int sm_count() {
-  static int counts[64];
-  const int dev = current_device();
-  if (dev < 0 || dev >= 64) return 152;
-  if (counts[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    counts[dev] = n;
-  }
-  return counts[dev];
 }
 
 // How many CTAs share the key range of each single-tile last block. Units are
@@ -304,7 +306,7 @@ int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* 
   }
   const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, min_kv));
   if (forced > 0) return std::max(1, std::min(forced, cap));
-  const int G = sm_count();
+  const int G = sr::sm_count();
   int best = 1;
   double best_t = 0;
   for (int k = 1; k <= cap; ++k) {
@@ -345,6 +347,18 @@ int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* 
 
 // ------------------------------------------------------------ allocation-free path
 namespace sr {
+
+int sm_count() {
+  static int counts[64];
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return 152;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
 
 int session_heads(const sr_session* s) { return s->cfg.n_heads; }
 
@@ -389,9 +403,11 @@ sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, con
   p.lse = lse;
   p.err_word = s->buf.err_word;
   p.timeout_ns = s->cfg.wait_timeout_ns;
-  return launch_attention_1(p, s->cfg.head_dim, n_units, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? SR_OK
-             : SR_ERR_CUDA;
+  s->buf.workspace = scratch;
+  set_units(p, n_units, s);
+  s->buf.workspace = own;
+  return launch_attention_1(p, s->cfg.head_dim, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SR_OK
+                                                                                                  : SR_ERR_CUDA;
 }
 
 }  // namespace sr
@@ -464,7 +480,8 @@ sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const vo
   }
   if (e == cudaSuccess)
     e = sr::launch_init_ring_state(bufs->slot_frame, cfg->window_frames, bufs->err_word,
-                                   static_cast<int32_t*>(bufs->workspace), cfg->n_heads, cs);
+                                   static_cast<int32_t*>(bufs->workspace),
+                                   static_cast<int>(sr::kWsUnitCtrBytes / 4) + cfg->n_heads, cs);
   if (e == cudaSuccess && bufs->frame_counter) {
     // device-state calls: the counter starts at 0, and ring tiles that straddle
     // the visible rows read zeros rather than whatever the buffers held
@@ -617,7 +634,8 @@ static sr_status attention_view(sr_session* s, const ChunkView& view, int32_t st
     p->lse = lse;
     p->err_word = s->buf.err_word;
     p->timeout_ns = s->cfg.wait_timeout_ns;
-    cudaError_t e = sr::launch_attention_1(*p, s->cfg.head_dim, n_units, static_cast<cudaStream_t>(stream));
+    set_units(*p, n_units, s);
+    cudaError_t e = sr::launch_attention_1(*p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) st = SR_ERR_CUDA;
   }
   delete p;
@@ -718,7 +736,8 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
     p->lse = lse;
     p->err_word = s->buf.err_word;
     p->timeout_ns = s->cfg.wait_timeout_ns;
-    cudaError_t e = sr::launch_attention_n(*p, s->cfg.head_dim, full + tails, static_cast<cudaStream_t>(stream));
+    p->n_units = full + tails;   // no workspace pointers here: one unit per CTA
+    cudaError_t e = sr::launch_attention_n(*p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) st = SR_ERR_CUDA;
   }
   delete p;
@@ -782,7 +801,8 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
     p->lse = lse;
     p->err_word = s0->buf.err_word;
     p->timeout_ns = s0->cfg.wait_timeout_ns;
-    cudaError_t e = sr::launch_attention_n(*p, s0->cfg.head_dim, units, static_cast<cudaStream_t>(stream));
+    set_units(*p, units, sessions[order[0]]);
+    cudaError_t e = sr::launch_attention_n(*p, s0->cfg.head_dim, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) st = SR_ERR_CUDA;
   }
   delete p;

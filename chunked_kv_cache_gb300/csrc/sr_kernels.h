@@ -77,6 +77,11 @@ struct alignas(128) AttnParams {
   float* lse;
   int32_t* err_word;
   uint64_t timeout_ns;
+  int32_t n_units;                // work units of the launch
+  int32_t epoch;                  // tags the unit counter (the first session's call epoch)
+  // Launch-wide unit counter and count of CTAs that ran out of units (two
+  // words in the first session's workspace). NULL: one unit per CTA.
+  unsigned long long* unit_ctr;
 };
 
 constexpr int kAttnThreads = 384;  // 2 softmax warpgroups, then MMA warp, TMA warp and 2 idle warps
@@ -84,9 +89,11 @@ constexpr int kAttnMaxBatch = SR_MAX_BATCH;
 
 int attn_smem_bytes(int head_dim);
 cudaError_t attn_prepare(int head_dim, int nsess_template);   // sets the smem attribute
-cudaError_t launch_attention_1(const AttnParams<1>& p, int head_dim, int n_units, cudaStream_t st);
-cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim, int n_units,
-                               cudaStream_t st);
+// Grid: one CTA per unit, or, with a unit counter, one CTA per SM (at most
+// one per unit) taking units until none are left.
+cudaError_t launch_attention_1(const AttnParams<1>& p, int head_dim, cudaStream_t st);
+cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim, cudaStream_t st);
+int sm_count();   // SMs of the current device
 
 // ------------------------------------------------------------ RoPE / commit
 struct RopeParams {
@@ -130,8 +137,12 @@ sr_status attention_scratch_check(const sr_session* s, int32_t step, const void*
 sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, const void* k, const void* v, void* o,
                                  float* lse, void* stream, void* scratch);
 int session_heads(const sr_session* s);
-// workspace layout: counters (padded to 256 B), then the partials
-inline size_t ws_counter_bytes(int n_heads) { return (static_cast<size_t>(n_heads) * 4 + 255) / 256 * 256; }
+// workspace layout: the launch-wide unit counter (two 64-bit words), the
+// per-head arrival counters (together padded to 256 B), then the partials
+constexpr size_t kWsUnitCtrBytes = 16;
+inline size_t ws_counter_bytes(int n_heads) {
+  return (kWsUnitCtrBytes + static_cast<size_t>(n_heads) * 4 + 255) / 256 * 256;
+}
 inline size_t ws_partial_floats_per_head(int head_dim) { return static_cast<size_t>(kMaxTailSplit) * 128 * (head_dim + 4); }
 cudaError_t launch_debug_wait(int32_t* err_word, uint64_t timeout_ns, cudaStream_t st);
 

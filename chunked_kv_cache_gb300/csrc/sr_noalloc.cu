@@ -33,7 +33,8 @@ constexpr uint64_t kScratchBytes = 16ull << 20;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
-// The per-head arrival counters sit at the start of the scratch.
+// The launch-wide unit counter and the per-head arrival counters sit at the
+// start of the scratch.
 __global__ void clear_arrival_counters(int n) {
   int32_t* ctr = reinterpret_cast<int32_t*>(g_attn_scratch);
   for (int i = threadIdx.x; i < n; i += blockDim.x) ctr[i] = 0;
@@ -68,7 +69,7 @@ sr_status sr_chunk_attention_noalloc(sr_session* s, int32_t step, const void* q,
   void* scratch = scratch_address();
   if (scratch == nullptr) return SR_ERR_CUDA;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  clear_arrival_counters<<<1, 256, 0, cs>>>(sr::session_heads(s));
+  clear_arrival_counters<<<1, 256, 0, cs>>>(static_cast<int>(sr::kWsUnitCtrBytes / 4) + sr::session_heads(s));
   if (cudaGetLastError() != cudaSuccess) return SR_ERR_CUDA;
   return sr::attention_into_scratch(s, step, q, k, v, o, lse, stream, scratch);
 }
