@@ -96,8 +96,9 @@ typedef struct {
   void* ring_v;             /* [W*T][H][d] bf16 */
   int32_t* slot_frame;      /* [W] int32: absolute frame held by each slot, -1 = empty */
   int32_t* err_word;        /* [1] int32: device error word (see SR_DEVERR_*) */
-  void* workspace;          /* optional, 256-byte aligned, sr_workspace_bytes() long: partial
-                               results of key-split last blocks. NULL disables the split. The
+  void* workspace;          /* optional, 256-byte aligned, sr_workspace_bytes() long: the work
+                               counter of persistent attention launches and the partial results of
+                               key-split last blocks. NULL: one CTA per work unit and no split. The
                                library initialises it in sr_session_init; do not modify it after. */
   int64_t* frame_counter;   /* optional [1] int64 device: the committed-frame count the *_dev calls
                                read and advance on the device (NULL: those calls are refused).
@@ -108,7 +109,8 @@ typedef struct {
 
 /*
  * Bytes of workspace a session with this config can use (see sr_buffers.workspace):
- * per head, SR_MAX_TAIL_SPLIT partial results of 128 rows plus a counter.
+ * a launch-wide work counter, and per head a counter and SR_MAX_TAIL_SPLIT partial
+ * results of 128 rows.
  */
 SR_API sr_status sr_workspace_bytes(const sr_config* cfg, uint64_t* bytes);
 
@@ -157,8 +159,11 @@ SR_API sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream);
  * bf16 operands, fp32 accumulation and fp32 online softmax on the tensor cores.
  * When the chunk's last 256-row query block holds a single 128-row tile and the
  * session has a workspace, that block's key range may be split over several CTAs
- * (sr_config.tail_split); the last CTA to finish merges the partial results. Calls
- * of one session that overlap on the GPU race on that workspace.
+ * (sr_config.tail_split); the last CTA to finish merges the partial results. With a
+ * workspace the launch is persistent (one CTA per SM taking work units from a counter
+ * in the workspace). Calls of one session that overlap on the GPU race on that
+ * workspace. After a device timeout (err_word set) initialise the session again: a
+ * CUDA-graph replay of the same launch could otherwise inherit a stale count.
  */
 SR_API sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, const void* k,
                              const void* v, void* o, float* lse, void* stream);
