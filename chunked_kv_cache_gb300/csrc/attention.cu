@@ -159,10 +159,12 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 
 template <int NSESS>
 __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, int H, int& si, int& head,
-                                            int& qb, int& part) {
+                                            int& qb, int& part, int& tile) {
   part = 0;
   si = 0;
-  if (u < p.n_full_units) {
+  tile = -1;   // the unit is a whole block or a last block
+  const int n_whole = p.n_full_units - p.n_conv;
+  if (u < n_whole) {
     // whole blocks, session by session, the blocks of one head next to each
     // other (they read the same keys and values, which then come from L2)
 #pragma unroll 1
@@ -171,10 +173,18 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
     const int nf = p.sess[si].nfull;
     head = local / nf;
     qb = local % nf;
+  } else if (u < p.n_full_units + p.n_conv) {
+    // the last n_conv whole blocks of a one-group launch, two single-tile units each
+    const int v = u - n_whole;
+    const int b = n_whole + v / 2;
+    tile = v % 2;
+    const int nf = p.sess[0].nfull;
+    head = b / nf;
+    qb = b % nf;
   } else {
     // single-tile last blocks (H per session that has them), each run as
     // tail_split key-range parts
-    const int t = u - p.n_full_units;
+    const int t = u - p.n_full_units - p.n_conv;
     const int tail = t / p.tail_split;
     part = t - tail * p.tail_split;
 #pragma unroll 1
@@ -189,8 +199,8 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
 // device-state call).
 template <int NSESS>
 __device__ __forceinline__ void make_unit(const AttnParams<NSESS>& p, int u, UnitRec& r) {
-  int si, head, qb, part;
-  decode_unit(p, u, p.n_heads, si, head, qb, part);
+  int si, head, qb, part, tile;
+  decode_unit(p, u, p.n_heads, si, head, qb, part, tile);
   const AttnSession& S = p.sess[si];
   TileMap tl;
 #pragma unroll
@@ -227,10 +237,10 @@ __device__ __forceinline__ void make_unit(const AttnParams<NSESS>& p, int u, Uni
   r.si = si;
   r.head = head;
   r.part = part;
-  r.q_local0 = qb * 2 * BM;
-  r.n_qtiles = min(2, (S.lq - r.q_local0 + BM - 1) / BM);
-  // a single-tile last block may be one of `parts` CTAs sharing its key range
-  r.parts = (r.n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
+  r.q_local0 = qb * 2 * BM + (tile > 0 ? BM : 0);
+  r.n_qtiles = tile >= 0 ? 1 : min(2, (S.lq - r.q_local0 + BM - 1) / BM);
+  // a single-tile last block may be one of `parts` units sharing its key range
+  r.parts = (tile < 0 && r.n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
   r.kv_lo = static_cast<int>(static_cast<int64_t>(part) * n_kv_all / r.parts);
   r.n_kv = static_cast<int>(static_cast<int64_t>(part + 1) * n_kv_all / r.parts) - r.kv_lo;
   r.tm = tl;

@@ -36,6 +36,8 @@ struct sr_session {
   float scale;
   int64_t n_committed;
   int32_t epoch;              // attention calls so far (key-split counters)
+  int64_t plan_key[4];        // the launch plan last chosen (choose_plan), and what it was chosen for
+  int32_t plan_split, plan_conv;
   double inv_freq[64];
   int8_t axis[64];
 };
@@ -284,7 +286,7 @@ int64_t key_tiles(const sr_session* s, const ChunkView& view) {
 // How many CTAs share the key range of each single-tile last block. Units are
 // dispatched in order (full blocks, then last-block parts) to whichever SM
 // frees up first, one CTA per SM; simulate that for 1..4 parts and keep the
-// shortest makespan, ties going to more parts. Costs in key-tile iterations
+// shortest makespan (more parts only when they gain at least 0.5 %). Costs in key-tile iterations
 // of a full block, measured on GB300: a full block walks all its key tiles; a
 // last-block part walks its share in split mode, half the tiles per query
 // tile at 1.33x the cost of a full-block iteration, plus about half an
@@ -335,17 +337,88 @@ int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* 
       t = std::max(t, free_at.top());
       free_at.pop();
     }
-    if (k == 1 || t <= best_t * 1.0001) {
+    if (k == 1 || t < best_t * 0.995) {   // more parts must gain clearly
       best = k;
-      best_t = std::min(best_t > 0 ? best_t : t, t);
+      best_t = t;
     }
   }
   return best;
 }
 
+// Launch plan of a one-group launch: key-range parts per single-tile last
+// block (k, as choose_tail_split) and how many of the last whole blocks run
+// as two single-tile units each (c). When the whole blocks do not fill the
+// last wave (n mod SMs of them left over), those few blocks would otherwise
+// run alone on as many SMs while the rest idle; as single-tile units (1.33x
+// the cost per tile, half the length) they spread over every SM. The same
+// dispatch simulation as choose_tail_split decides, for c in {0, that
+// remainder}; the result is kept per session for the shape it was made for.
+void choose_plan(sr_session* s, const ChunkView& view, int& k_out, int& c_out) {
+  const int G = sr::sm_count();
+  const int64_t tiles = key_tiles(s, view);
+  const int64_t key[4] = {view.lq, tiles, G, s->buf.workspace != nullptr};
+  if (std::equal(key, key + 4, s->plan_key)) {
+    k_out = s->plan_split;
+    c_out = s->plan_conv;
+    return;
+  }
+  const int H = s->cfg.n_heads;
+  const int64_t rem = view.lq % 256;
+  const bool single = rem > 0 && rem <= 128;
+  const int64_t whole = static_cast<int64_t>(H) * ((view.lq + 255) / 256 - (single ? 1 : 0));
+  int k_lo = 1, k_hi = 1;
+  if (single && s->buf.workspace) {
+    const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, tiles));
+    const int forced = s->cfg.tail_split;
+    k_lo = forced > 0 ? std::max(1, std::min(forced, cap)) : 1;
+    k_hi = forced > 0 ? k_lo : cap;
+  }
+  const int64_t left = whole % G;
+  const double full_cost = static_cast<double>(tiles);
+  const double single_cost = std::ceil(tiles / 2.0) * 1.33 + 0.5;
+  int best_k = k_lo, best_c = 0;
+  double best_t = 0;
+  bool have = false;
+  for (int64_t c : {int64_t(0), left}) {
+    if (have && c == 0) break;   // left == 0: nothing to convert
+    for (int k = k_lo; k <= k_hi; ++k) {
+      std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+      for (int g = 0; g < G; ++g) free_at.push(0.0);
+      auto run = [&](double cost) {
+        const double t0 = free_at.top();
+        free_at.pop();
+        free_at.push(t0 + cost);
+      };
+      for (int64_t u = 0; u < whole - c; ++u) run(full_cost);
+      for (int64_t u = 0; u < 2 * c; ++u) run(single_cost);
+      if (single) {
+        const double part = std::ceil(std::ceil(tiles / static_cast<double>(k)) / 2.0) * 1.33 + 0.5 + (k > 1 ? 0.5 : 0.0);
+        for (int64_t u = 0; u < static_cast<int64_t>(H) * k; ++u) run(part);
+      }
+      double t = 0;
+      while (!free_at.empty()) {
+        t = std::max(t, free_at.top());
+        free_at.pop();
+      }
+      // more parts or a conversion must gain clearly: each part and unit costs set-up
+      const bool better = !have || (c == best_c ? t < best_t * 0.995 : t < best_t * 0.98);
+      if (better) {
+        best_t = t;
+        best_k = k;
+        best_c = static_cast<int>(c);
+        have = true;
+      }
+    }
+  }
+  std::copy(key, key + 4, s->plan_key);
+  s->plan_split = best_k;
+  s->plan_conv = best_c;
+  k_out = best_k;
+  c_out = best_c;
+}
+
 }  // namespace
 
-// ------------------------------------------------------------ allocation-free path
 namespace sr {
 
 int sm_count() {
@@ -386,15 +459,16 @@ sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, con
   s->buf.workspace = scratch;
   const ChunkView view = default_view(s);
   sr_status st = fill_session(p.sess[0], s, view, step, k, v, 0);
-  const int order0 = 0;
-  const int split = st == SR_OK ? choose_tail_split(&s, &view, &order0, 1) : 1;
+  int split = 1, conv = 0;
+  if (st == SR_OK) choose_plan(s, view, split, conv);
   s->buf.workspace = own;
   if (st != SR_OK) return st;
   int full = 0, tails = 0;
   place_units(p.sess[0], s->cfg.n_heads, full, tails);
   p.n_full_units = full;
+  p.n_conv = conv;
   p.tail_split = split;
-  const int n_units = full + tails * split;
+  const int n_units = full + conv + tails * split;
   p.n_sess = 1;
   p.n_heads = s->cfg.n_heads;
   p.scale_log2 = s->scale * 1.4426950408889634f;
@@ -623,9 +697,11 @@ static sr_status attention_view(sr_session* s, const ChunkView& view, int32_t st
     int full = 0, tails = 0;
     place_units(p->sess[0], s->cfg.n_heads, full, tails);
     p->n_full_units = full;
-    const int order0 = 0;
-    p->tail_split = choose_tail_split(&s, &view, &order0, 1);
-    n_units = full + tails * p->tail_split;
+    int split = 1, conv = 0;
+    choose_plan(s, view, split, conv);
+    p->n_conv = conv;
+    p->tail_split = split;
+    n_units = full + conv + tails * split;
     p->n_sess = 1;
     p->n_heads = s->cfg.n_heads;
     p->scale_log2 = s->scale * 1.4426950408889634f;
