@@ -30,6 +30,7 @@ EXPORTS = (
     "sr_chunk_attention_noalloc", "sr_plan_chunk", "sr_rope3d_qk_frames", "sr_chunk_attention_frames",
     "sr_cache_commit_frames", "sr_window_attention", "sr_rope3d_qk_at", "sr_rope3d_qk_dev",
     "sr_chunk_attention_dev", "sr_cache_commit_dev", "sr_window_count", "sr_plan_window",
+    "sr_plan_attention",
 )
 
 
@@ -106,6 +107,8 @@ def lib() -> ctypes.CDLL:
         L.sr_plan_window.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(SrWindow)]
         L.sr_chunk_attention_batch.argtypes = [ctypes.POINTER(vp), i32, i32, vp, vp, vp,
                                                ctypes.POINTER(i64), vp, vp, vp]
+        L.sr_plan_attention.argtypes = [i32, i64, i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                        ctypes.POINTER(i64)]
         L.sr_device_error_status.argtypes = [i32]
         L.sr_debug_wait_timeout.argtypes = [vp, u64, vp]
         L.sr_workspace_bytes.argtypes = [ctypes.POINTER(SrConfig), ctypes.POINTER(ctypes.c_uint64)]
@@ -166,6 +169,16 @@ def sr_plan_chunk(chunk_index: int, bootstrap_units: int = 7, chunk_units: int =
                                int(sink_units), 1 if merge_single_frame_units else 0, ctypes.byref(out)),
            "sr_plan_chunk")
     return out
+
+
+def sr_plan_attention(n_heads: int, lq: int, key_tiles: int, has_workspace: bool = True, tail_split: int = 0,
+                      sm_count: int = 0) -> dict:
+    """The attention launch plan of one query group (host arithmetic)."""
+    parts, conv, units = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+    _check(lib().sr_plan_attention(int(n_heads), int(lq), int(key_tiles), 1 if has_workspace else 0, int(tail_split),
+                                   int(sm_count), ctypes.byref(parts), ctypes.byref(conv), ctypes.byref(units)),
+           "sr_plan_attention")
+    return {"parts": parts.value, "whole_as_tiles": conv.value, "n_units": units.value}
 
 
 def sr_rope3d_qk_frames(handle: int, n_frames: int, q: int, k: int, stream: int) -> None:

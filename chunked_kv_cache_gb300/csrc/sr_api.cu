@@ -353,23 +353,14 @@ int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* 
 // the cost per tile, half the length) they spread over every SM. The same
 // dispatch simulation as choose_tail_split decides, for c in {0, that
 // remainder}; the result is kept per session for the shape it was made for.
-void choose_plan(sr_session* s, const ChunkView& view, int& k_out, int& c_out) {
-  const int G = sr::sm_count();
-  const int64_t tiles = key_tiles(s, view);
-  const int64_t key[4] = {view.lq, tiles, G, s->buf.workspace != nullptr};
-  if (std::equal(key, key + 4, s->plan_key)) {
-    k_out = s->plan_split;
-    c_out = s->plan_conv;
-    return;
-  }
-  const int H = s->cfg.n_heads;
-  const int64_t rem = view.lq % 256;
+// The plan itself, from the launch's numbers alone.
+void plan_units(int H, int64_t lq, int64_t tiles, bool has_ws, int forced, int G, int& k_out, int& c_out) {
+  const int64_t rem = lq % 256;
   const bool single = rem > 0 && rem <= 128;
-  const int64_t whole = static_cast<int64_t>(H) * ((view.lq + 255) / 256 - (single ? 1 : 0));
+  const int64_t whole = static_cast<int64_t>(H) * ((lq + 255) / 256 - (single ? 1 : 0));
   int k_lo = 1, k_hi = 1;
-  if (single && s->buf.workspace) {
+  if (single && has_ws) {
     const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, tiles));
-    const int forced = s->cfg.tail_split;
     k_lo = forced > 0 ? std::max(1, std::min(forced, cap)) : 1;
     k_hi = forced > 0 ? k_lo : cap;
   }
@@ -410,11 +401,21 @@ void choose_plan(sr_session* s, const ChunkView& view, int& k_out, int& c_out) {
       }
     }
   }
-  std::copy(key, key + 4, s->plan_key);
-  s->plan_split = best_k;
-  s->plan_conv = best_c;
   k_out = best_k;
   c_out = best_c;
+}
+
+void choose_plan(sr_session* s, const ChunkView& view, int& k_out, int& c_out) {
+  const int G = sr::sm_count();
+  const int64_t tiles = key_tiles(s, view);
+  const int64_t key[4] = {view.lq, tiles, G, s->buf.workspace != nullptr};
+  if (!std::equal(key, key + 4, s->plan_key)) {
+    plan_units(s->cfg.n_heads, view.lq, tiles, s->buf.workspace != nullptr, s->cfg.tail_split, G, s->plan_split,
+               s->plan_conv);
+    std::copy(key, key + 4, s->plan_key);
+  }
+  k_out = s->plan_split;
+  c_out = s->plan_conv;
 }
 
 }  // namespace
@@ -502,6 +503,24 @@ const char* sr_status_string(sr_status st) {
 }
 
 sr_status sr_device_error_status(int32_t v) { return v == SR_DEVERR_NONE ? SR_OK : SR_ERR_TIMEOUT; }
+
+sr_status sr_plan_attention(int32_t n_heads, int64_t lq, int64_t key_tiles, int32_t has_workspace,
+                            int32_t tail_split, int32_t sm_count, int32_t* parts, int32_t* whole_as_tiles,
+                            int64_t* n_units) {
+  if (!parts || !whole_as_tiles || !n_units || n_heads < 1 || lq < 1 || key_tiles < 1 || tail_split < 0 ||
+      tail_split > SR_MAX_TAIL_SPLIT || lq > (int64_t(1) << 28) || key_tiles > (int64_t(1) << 24))
+    return SR_ERR_INVALID_ARG;
+  const int G = sm_count > 0 ? sm_count : sr::sm_count();
+  int k = 1, c = 0;
+  plan_units(n_heads, lq, key_tiles, has_workspace != 0, tail_split, G, k, c);
+  const int64_t rem = lq % 256;
+  const bool single = rem > 0 && rem <= 128;
+  const int64_t whole = static_cast<int64_t>(n_heads) * ((lq + 255) / 256 - (single ? 1 : 0));
+  *parts = k;
+  *whole_as_tiles = c;
+  *n_units = whole + c + (single ? static_cast<int64_t>(n_heads) * k : 0);
+  return SR_OK;
+}
 
 sr_status sr_workspace_bytes(const sr_config* cfg, uint64_t* bytes) {
   if (!cfg || !bytes) return SR_ERR_INVALID_ARG;

@@ -115,6 +115,22 @@ typedef struct {
 SR_API sr_status sr_workspace_bytes(const sr_config* cfg, uint64_t* bytes);
 
 /*
+ * The plan sr_chunk_attention uses for one query group (host arithmetic only; no
+ * device is needed when sm_count > 0): lq query rows over key_tiles 128-row key
+ * tiles, n_heads heads. The launch runs whole 256-row blocks first, then the
+ * single-tile last blocks (lq mod 256 in 1..128), each split into *parts key-range
+ * parts (needs a workspace; tail_split > 0 forces the count, clamped to 1..key_tiles
+ * and SR_MAX_TAIL_SPLIT). *whole_as_tiles of the last whole blocks run as two
+ * single-tile units each, to balance a partly filled last wave of sm_count SMs
+ * (<= 0: the current device's). The choice comes from simulating the dispatch of
+ * the units, longest first, to the SM that frees up first. *n_units: units of the
+ * launch. SR_ERR_INVALID_ARG for NULL outputs or sizes out of range.
+ */
+SR_API sr_status sr_plan_attention(int32_t n_heads, int64_t lq, int64_t key_tiles, int32_t has_workspace,
+                                   int32_t tail_split, int32_t sm_count, int32_t* parts, int32_t* whole_as_tiles,
+                                   int64_t* n_units);
+
+/*
  * Create a session. Copies the sink banks from sink_k_src / sink_v_src (device,
  * same layout as the bank) into bufs->sink_k / sink_v when they are non-NULL
  * (NULL: the bank already holds them), fills slot_frame with -1, clears

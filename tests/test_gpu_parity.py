@@ -122,6 +122,24 @@ def test_attention_832x480_full(fill):
     assert np.abs(gl - rl).max() <= LSE_ABS
 
 
+@pytest.mark.parametrize("gh,gw", [
+    (8, 16),    # Lq 256: one block of two tiles, no last-block units
+    (10, 16),   # Lq 320: a single-tile last block of 64 rows
+    (12, 16),   # Lq 384: a single-tile last block of exactly 128 rows
+    (13, 16),   # Lq 416: a last block of two tiles (128 + 32 rows) runs as a whole block
+    (16, 32),   # Lq 1024: four whole blocks per head, side by side
+])
+@pytest.mark.parametrize("workspace", [True, False])
+def test_attention_block_shapes(gh, gw, workspace):
+    shape = syn.Shape(f"blocks {gh}x{gw}", 3, 128, gh, gw, 2, 2, 40)
+    tw = Twin(shape, 1, fill=2, workspace=workspace)
+    x = syn.chunk_inputs(shape, 1, chunk=3)
+    got, ref, gl, rl = tw.step(x, 0, lse=True)
+    assert_attention_close(got, ref, f"blocks {gh}x{gw}")
+    assert np.abs(gl - rl).max() <= LSE_ABS
+    assert tw.gpu.error_status() == 0
+
+
 def _edge_rows(lq):
     base = [0, 1, 126, 127, 128, 129, 255, 256, 257, 511, 512, lq // 2, lq - 129, lq - 128, lq - 2, lq - 1]
     rng = np.random.default_rng(5)

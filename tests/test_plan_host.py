@@ -71,3 +71,72 @@ def test_c_window_planner_rejects_invalid(sr):
     assert N.lib().sr_window_count(8, 8, 4, 2, ctypes.byref(n)) == N.SR_ERR_INVALID_ARG   # shifted must be 0 or 1
     with pytest.raises(N.SrError):
         N.sr_plan_window(8, 8, 4, 0, 4)
+
+
+# ---------------------------------------------------------------- attention launch plan
+
+def _dispatch(costs, sms):
+    """Longest-first list scheduling: each unit to the SM that frees up first."""
+    import heapq
+    free = [0.0] * sms
+    for c in costs:
+        t = heapq.heappop(free)
+        heapq.heappush(free, t + c)
+    return max(free)
+
+
+def _plan_model(H, lq, tiles, ws, forced, sms):
+    """The plan restated: whole blocks, then single-tile units, then last-block parts."""
+    import math
+    rem = lq % 256
+    single = 0 < rem <= 128
+    whole = H * ((lq + 255) // 256 - (1 if single else 0))
+    ks = [1]
+    if single and ws:
+        cap = min(4, tiles)
+        ks = [max(1, min(forced, cap))] if forced else list(range(1, cap + 1))
+    best = None
+    for c in ([0, whole % sms] if whole % sms else [0]):
+        for k in ks:
+            costs = [float(tiles)] * (whole - c) + [math.ceil(tiles / 2) * 1.33 + 0.5] * (2 * c)
+            if single:
+                costs += [math.ceil(math.ceil(tiles / k) / 2) * 1.33 + 0.5 + (0.5 if k > 1 else 0)] * (H * k)
+            t = _dispatch(costs, sms)
+            if best is None or (c == best[2] and t < best[0] * 0.995) or (c != best[2] and t < best[0] * 0.98):
+                best = (t, k, c)
+    _, k, c = best
+    return {"parts": k, "whole_as_tiles": c, "n_units": whole + c + (H * k if single else 0)}
+
+
+@pytest.mark.parametrize("H,lq,tiles,want", [
+    (24, 3120, 114, {"parts": 2, "whole_as_tiles": 0, "n_units": 288 + 48}),     # 832x480, ring full
+    (40, 7200, 315, {"parts": 1, "whole_as_tiles": 56, "n_units": 1120 + 56 + 40}),   # 720p: 1120 = 7 x 152 + 56
+    (24, 4680, 78, {"parts": 1, "whole_as_tiles": 0, "n_units": 432 + 24}),
+])
+def test_attention_plan_workloads(sr, H, lq, tiles, want):
+    from chunked_kv_cache_gb300 import _native as N
+    assert N.sr_plan_attention(H, lq, tiles, True, 0, 152) == want
+    assert _plan_model(H, lq, tiles, True, 0, 152) == want
+
+
+def test_attention_plan_matches_model_on_small_launches(sr):
+    from chunked_kv_cache_gb300 import _native as N
+    import random
+    rng = random.Random(3)
+    for _ in range(300):
+        H, lq, tiles = rng.randint(1, 12), rng.randint(1, 2000), rng.randint(1, 40)
+        ws, forced, sms = rng.random() < 0.7, rng.choice([0, 0, 1, 2, 3, 4]), rng.choice([4, 16, 152])
+        assert N.sr_plan_attention(H, lq, tiles, ws, forced, sms) == _plan_model(H, lq, tiles, ws, forced, sms), \
+            (H, lq, tiles, ws, forced, sms)
+
+
+def test_attention_plan_without_workspace_and_invalid(sr):
+    from chunked_kv_cache_gb300 import _native as N
+    assert N.sr_plan_attention(24, 3120, 114, False, 0, 152)["parts"] == 1
+    assert N.sr_plan_attention(24, 3120, 114, True, 3, 152)["parts"] == 3
+    assert N.sr_plan_attention(24, 3120, 2, True, 4, 152)["parts"] == 2          # clamped to the key tiles
+    for args in [(0, 3120, 114), (24, 0, 114), (24, 3120, 0)]:
+        with pytest.raises(RuntimeError):
+            N.sr_plan_attention(*args)
+    with pytest.raises(RuntimeError):
+        N.sr_plan_attention(24, 3120, 114, True, 5, 152)
