@@ -600,7 +600,7 @@ def run_window(args):
     for sid in range(2):
         sink = lambda tid: syn.device_normal_bf16((base.n_steps, S, H, d), dev, 6, sid, 0, 0, tid)
         s = sr.Session(H, d, base.grid_h, base.grid_w, 3, 0, S, base.n_steps, sink_k=sink(syn.T_SINK_K),
-                       sink_v=sink(syn.T_SINK_V), workspace=False, device=dev)
+                       sink_v=sink(syn.T_SINK_V), device=dev)
         x = {k: [syn.device_normal_bf16((M, H, d), dev, 6, sid, 1, st, tid) for st in range(base.n_steps)]
              for k, tid in (("q", syn.T_Q), ("k", syn.T_K), ("v", syn.T_V))}
         x["o"] = torch.empty((M, H, d), dtype=torch.bfloat16, device=dev)

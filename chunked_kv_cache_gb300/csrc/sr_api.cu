@@ -233,6 +233,14 @@ const char* bank_ptr(const void* bank, const sr_session* s, int step) {
   return static_cast<const char*>(bank) + static_cast<size_t>(step) * s->cfg.n_sink * row_bytes;
 }
 
+// A new epoch for this call's counters (27 bits: the key-split counter keeps
+// its arrivals in the low 4 bits of an int32; never 0, the cleared value).
+int32_t next_epoch(sr_session* s) {
+  s->epoch = (s->epoch + 1) & 0x07FFFFFF;
+  if (s->epoch == 0) s->epoch = 1;
+  return s->epoch;
+}
+
 // Fill one session's segment maps for `step` (rows of the chunk taken from
 // k, v at row offset `row0` of a packed tensor).
 sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& view, int step, const void* k,
@@ -265,9 +273,7 @@ sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& vie
     char* ws = static_cast<char*>(s->buf.workspace);
     out.ws_ctr = reinterpret_cast<int32_t*>(ws + sr::kWsUnitCtrBytes);
     out.ws_part = reinterpret_cast<float*>(ws + sr::ws_counter_bytes(s->cfg.n_heads));
-    s->epoch = (s->epoch + 1) & 0x07FFFFFF;
-    if (s->epoch == 0) s->epoch = 1;
-    out.epoch = s->epoch;
+    out.epoch = next_epoch(s);
   }
   return SR_OK;
 }
@@ -831,7 +837,20 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
     p->lse = lse;
     p->err_word = s->buf.err_word;
     p->timeout_ns = s->cfg.wait_timeout_ns;
-    p->n_units = full + tails;   // no workspace pointers here: one unit per CTA
+    // no key-range parts (the groups share one session); with a workspace the
+    // launch is persistent, and a one-group launch may balance its last wave
+    int conv = 0;
+    if (n == 1) {
+      int k = 1;
+      const int64_t tiles = (s->cfg.n_sink + 127) / 128 + (M + 127) / 128;
+      plan_units(s->cfg.n_heads, M, tiles, false, 0, sr::sm_count(), k, conv);
+    }
+    p->n_conv = conv;
+    p->n_units = full + conv + tails;
+    if (s->buf.workspace) {
+      p->unit_ctr = static_cast<unsigned long long*>(s->buf.workspace);
+      p->epoch = next_epoch(s);
+    }
     cudaError_t e = sr::launch_attention_n(*p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) st = SR_ERR_CUDA;
   }
