@@ -791,19 +791,31 @@ def run_decoder(args):
             for _ in range(max(args.warmup, 3)):
                 lay.attention(q, k, v, out=o)
             torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            for _ in range(args.steps):
+            def timed(fn):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(args.steps):
+                    fn()
+                b.record()
+                torch.cuda.synchronize()
+                return a.elapsed_time(b) / args.steps
+            eager_ms = timed(lambda: lay.attention(q, k, v, out=o))
+            # the same layer replayed from a CUDA graph: the device time without
+            # the host's per-call work (16 windows' tensor maps per launch)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
                 lay.attention(q, k, v, out=o)
-            b.record()
+            for _ in range(3):
+                g.replay()
             torch.cuda.synchronize()
-            ms = a.elapsed_time(b) / args.steps
+            ms = timed(g.replay)
             fl = sum(4.0 * H * s.lq * (G + 6 * s.T) * d for s in lay.sessions)
             full = [s for s in lay.sessions if s.T == 256]
             lay_fl[f"{gname}, {'shifted' if shifted else 'plain'} layer"] = fl
             results[f"{gname}, {'shifted' if shifted else 'plain'} layer"] = {
                 "windows": len(lay.windows), "full_windows": len(full), "launches": len(lay.groups),
-                "ms_per_layer": round(ms, 4), "tflops": round(fl / (ms / 1e3) / 1e12, 2)}
+                "ms_per_layer": round(ms, 4), "tflops": round(fl / (ms / 1e3) / 1e12, 2),
+                "eager_ms_per_layer": round(eager_ms, 4)}
             if lay.error_status() != 0:
                 raise RuntimeError("device error word set during the bench")
             lay.close()
@@ -815,7 +827,8 @@ def run_decoder(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "streaming decoder layer: 16x16-token windows, 2-frame chunk, 4 cached frames, "
                                "5 global tokens, 16 heads x 128 (synthetic); windows batched per launch "
-                               "(at most 16); full cache; attention only"},
+                               "(at most 16); full cache; attention only; ms_per_layer from a CUDA-graph "
+                               "replay of the layer's launches (eager_ms_per_layer: issued call by call)"},
         "layers": results,
         "context": "pages: FlexAttention with a block mask, 6 ms per layer on GB200 (their 1.62B decoder)",
         "roofline": {"bound": "tensor", "achieved": results[key]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
@@ -824,7 +837,7 @@ def run_decoder(args):
         "cpu_baseline": _oracle_line(rate, done, used, "one full window (512 queries x 1541 keys); ms per layer "
                                      "extrapolated to every window and head of the " + key,
                                      value=round(lay_fl[key] / rate * 1e3, 2), unit="ms/layer"),
-        "gpu_launches": sum(v["launches"] for v in results.values()) * args.steps,
+        "gpu_launches": 2 * sum(v["launches"] for v in results.values()) * args.steps,
     }
     print(json.dumps(out), flush=True)
 

@@ -174,13 +174,16 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
     head = local / nf;
     qb = local % nf;
   } else if (u < p.n_full_units + p.n_conv) {
-    // the last n_conv whole blocks of a one-group launch, two single-tile units each
+    // the last n_conv whole blocks, two single-tile units each
     const int v = u - n_whole;
     const int b = n_whole + v / 2;
     tile = v % 2;
-    const int nf = p.sess[0].nfull;
-    head = b / nf;
-    qb = b % nf;
+#pragma unroll 1
+    while (si + 1 < p.n_sess && b >= p.sess[si].unit_begin + H * p.sess[si].nfull) ++si;
+    const int local = b - p.sess[si].unit_begin;
+    const int nf = p.sess[si].nfull;
+    head = local / nf;
+    qb = local % nf;
   } else {
     // single-tile last blocks (H per session that has them), each run as
     // tail_split key-range parts

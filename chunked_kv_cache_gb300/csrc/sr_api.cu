@@ -40,6 +40,15 @@ struct sr_session {
   int32_t plan_split, plan_conv;
   double inv_freq[64];
   int8_t axis[64];
+  // Tensor maps encoded for this session's calls, by (address, rows): a map
+  // holds only the address, extents and strides, so a buffer that comes back
+  // (the banks, the ring, a caller's reused chunk buffers) reuses its map.
+  struct MapEntry {
+    const void* base;
+    int64_t rows;
+    CUtensorMap map;
+  } maps[16];
+  int32_t map_next;
 };
 
 namespace {
@@ -121,6 +130,23 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t row_e
   return r == CUDA_SUCCESS;
 }
 
+// encode_rows through the session's map cache (s may be NULL: no cache).
+bool encode_cached(sr_session* s, CUtensorMap* map, const void* base, int64_t rows, int64_t row_elems) {
+  if (s == nullptr) return encode_rows(map, base, rows, row_elems);
+  for (const auto& e : s->maps)
+    if (e.base == base && e.rows == rows && base != nullptr) {
+      *map = e.map;
+      return true;
+    }
+  if (!encode_rows(map, base, rows, row_elems)) return false;
+  auto& e = s->maps[s->map_next];
+  s->map_next = (s->map_next + 1) % 16;
+  e.base = base;
+  e.rows = rows;
+  e.map = *map;
+  return true;
+}
+
 int current_device() {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -188,12 +214,12 @@ struct Segment {
 // Encode a query group's four key/value segments (empty ones get no map),
 // and its query rows [row0, row0 + lq) of the packed q / o.
 sr_status encode_group(sr::AttnSession& out, const Segment (&seg)[sr::kSegs], int64_t row_elems, int64_t row0,
-                       int64_t lq) {
+                       int64_t lq, sr_session* cache) {
   std::memset(&out, 0, sizeof(out));
   for (int i = 0; i < sr::kSegs; ++i) {
     out.seg_rows[i] = static_cast<int32_t>(seg[i].rows);
-    if (seg[i].rows > 0 && (!encode_rows(&out.kmap[i], seg[i].k, seg[i].rows, row_elems) ||
-                            !encode_rows(&out.vmap[i], seg[i].v, seg[i].rows, row_elems)))
+    if (seg[i].rows > 0 && (!encode_cached(cache, &out.kmap[i], seg[i].k, seg[i].rows, row_elems) ||
+                            !encode_cached(cache, &out.vmap[i], seg[i].v, seg[i].rows, row_elems)))
       return SR_ERR_CUDA;
   }
   out.q_row0 = static_cast<int32_t>(row0);
@@ -261,7 +287,7 @@ sr_status fill_session(sr::AttnSession& out, sr_session* s, const ChunkView& vie
       {s->buf.ring_k, s->buf.ring_v, c1},
       {static_cast<const char*>(k) + static_cast<size_t>(row0) * row_bytes,
        static_cast<const char*>(v) + static_cast<size_t>(row0) * row_bytes, view.lq}};
-  sr_status st = encode_group(out, seg, row_elems, row0, view.lq);
+  sr_status st = encode_group(out, seg, row_elems, row0, view.lq, s);
   if (st != SR_OK) return st;
   if (view.dev) {
     out.dev_n = s->buf.frame_counter;
@@ -289,77 +315,113 @@ int64_t key_tiles(const sr_session* s, const ChunkView& view) {
   return n;
 }
 
-// How many CTAs share the key range of each single-tile last block. Units are
-// dispatched in order (full blocks, then last-block parts) to whichever SM
-// frees up first, one CTA per SM; simulate that for 1..4 parts and keep the
-// shortest makespan (more parts only when they gain at least 0.5 %). Costs in key-tile iterations
-// of a full block, measured on GB300: a full block walks all its key tiles; a
-// last-block part walks its share in split mode, half the tiles per query
-// tile at 1.33x the cost of a full-block iteration, plus about half an
-// iteration of set-up and, when split, half an iteration of merge.
-int choose_tail_split(sr_session* const* ss, const ChunkView* views, const int* order, int n) {
-  const int forced = ss[0]->cfg.tail_split;
-  auto single_tail = [&](int r) {   // the query group's last block is a single tile
-    const int64_t rem = views[order[r]].lq % 256;
-    return rem > 0 && rem <= 128;
-  };
-  // Only when every query group ends in a single tile: in a batch that mixes
-  // them (the decoder's edge windows), parts of the few short last blocks
-  // cost more in per-CTA set-up than they save.
+// Longest-first dispatch of units with the given costs (in key-tile
+// iterations of a whole block) to whichever of G SMs frees up first; the
+// makespan.
+double dispatch_makespan(const std::vector<double>& costs, int G) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int g = 0; g < G; ++g) free_at.push(0.0);
+  for (double c : costs) {
+    const double t0 = free_at.top();
+    free_at.pop();
+    free_at.push(t0 + c);
+  }
+  double t = 0;
+  while (!free_at.empty()) {
+    t = std::max(t, free_at.top());
+    free_at.pop();
+  }
+  return t;
+}
+
+// Whole blocks left over in a last wave that is at most half full (0 when
+// the blocks do not fill one wave, or fill the last one more than half): the
+// candidates for running as single-tile units. A launch smaller than a wave
+// shares the GPU with the previous and next launches of the stream, which the
+// simulation does not see, and a fuller last wave is better left whole
+// (measured on the decoder's shifted layers: converting them made a layer up
+// to 15 % slower).
+int64_t sparse_last_wave(int64_t whole, int G) {
+  if (whole < G) return 0;
+  const int64_t left = whole % G;
+  return left <= G / 2 ? left : 0;
+}
+
+// Costs measured on GB300, in iterations of a whole block: a whole block
+// walks all its key tiles; a single-tile unit walks half of them in split
+// mode at 1.33x the cost per tile, plus about half an iteration of set-up;
+// a key-range part of a last block walks its share the same way, plus half
+// an iteration of merge when the block is split.
+double single_tile_cost(double tiles) { return std::ceil(tiles / 2.0) * 1.33 + 0.5; }
+double part_cost(double tiles, int k) {
+  return std::ceil(std::ceil(tiles / k) / 2.0) * 1.33 + 0.5 + (k > 1 ? 0.5 : 0.0);
+}
+
+// The launch plan of a batch of query groups (in unit order): key-range parts
+// per single-tile last block (k; only when every group ends in a single tile
+// and has a workspace: in a batch that mixes them, such as the decoder's edge
+// windows, parts of the few short last blocks cost more in set-up than they
+// save) and how many of the last whole blocks run as two single-tile units
+// each (c; when the whole blocks leave a partly filled last wave, those few
+// blocks would otherwise run alone while the other SMs idle). The dispatch
+// simulation decides; more parts must shorten the makespan by 0.5 %, a
+// conversion by 2 %.
+void choose_batch_plan(sr_session* const* ss, const ChunkView* views, const int* order, int n, int& k_out,
+                       int& c_out) {
+  const int G = sr::sm_count();
+  const int forced = ss[order[0]]->cfg.tail_split;
+  std::vector<double> whole, tails;   // whole-block costs in unit order; tiles of each single-tile last block
+  bool all_single = true;
   int64_t min_kv = INT64_MAX;
   for (int r = 0; r < n; ++r) {
     const sr_session* s = ss[order[r]];
-    if (!single_tail(r) || !s->buf.workspace) return 1;
-    min_kv = std::min(min_kv, key_tiles(s, views[order[r]]));
+    const ChunkView& view = views[order[r]];
+    const int64_t rem = view.lq % 256;
+    const bool single = rem > 0 && rem <= 128;
+    const double tiles = static_cast<double>(key_tiles(s, view));
+    const int64_t blocks = static_cast<int64_t>(s->cfg.n_heads) * ((view.lq + 255) / 256 - (single ? 1 : 0));
+    whole.insert(whole.end(), static_cast<size_t>(blocks), tiles);
+    if (single) {
+      tails.insert(tails.end(), static_cast<size_t>(s->cfg.n_heads), tiles);
+      min_kv = std::min(min_kv, key_tiles(s, view));
+    }
+    if (!single || !s->buf.workspace) all_single = false;
   }
-  const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, min_kv));
-  if (forced > 0) return std::max(1, std::min(forced, cap));
-  const int G = sr::sm_count();
-  int best = 1;
+  int k_lo = 1, k_hi = 1;
+  if (all_single && !tails.empty()) {
+    const int cap = static_cast<int>(std::min<int64_t>(SR_MAX_TAIL_SPLIT, min_kv));
+    k_lo = forced > 0 ? std::max(1, std::min(forced, cap)) : 1;
+    k_hi = forced > 0 ? k_lo : cap;
+  }
+  const int64_t left = sparse_last_wave(static_cast<int64_t>(whole.size()), G);
+  int best_k = k_lo, best_c = 0;
   double best_t = 0;
-  for (int k = 1; k <= cap; ++k) {
-    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-    for (int g = 0; g < G; ++g) free_at.push(0.0);
-    auto run = [&](double cost) {
-      const double t0 = free_at.top();
-      free_at.pop();
-      free_at.push(t0 + cost);
-    };
-    for (int r = 0; r < n; ++r) {
-      const sr_session* s = ss[order[r]];
-      const ChunkView& view = views[order[r]];
-      const int64_t units = static_cast<int64_t>(s->cfg.n_heads) * ((view.lq + 255) / 256 - 1);
-      const double cost = static_cast<double>(key_tiles(s, view));
-      for (int64_t u = 0; u < units; ++u) run(cost);
-    }
-    for (int r = 0; r < n; ++r) {
-      const sr_session* s = ss[order[r]];
-      const double tiles = static_cast<double>(key_tiles(s, views[order[r]]));
-      const double part = std::ceil(std::ceil(tiles / k) / 2.0) * 1.33 + 0.5 + (k > 1 ? 0.5 : 0.0);
-      for (int64_t u = 0; u < static_cast<int64_t>(s->cfg.n_heads) * k; ++u) run(part);
-    }
-    double t = 0;
-    while (!free_at.empty()) {
-      t = std::max(t, free_at.top());
-      free_at.pop();
-    }
-    if (k == 1 || t < best_t * 0.995) {   // more parts must gain clearly
-      best = k;
-      best_t = t;
+  bool have = false;
+  std::vector<double> units;
+  for (int64_t c : {int64_t(0), left}) {
+    if (have && c == 0) break;   // left == 0: nothing to convert
+    for (int k = k_lo; k <= k_hi; ++k) {
+      units.clear();
+      const size_t keep = whole.size() - static_cast<size_t>(c);
+      units.insert(units.end(), whole.begin(), whole.begin() + static_cast<std::ptrdiff_t>(keep));
+      for (size_t i = keep; i < whole.size(); ++i) units.insert(units.end(), 2, single_tile_cost(whole[i]));
+      for (double t : tails) units.insert(units.end(), static_cast<size_t>(k), part_cost(t, k));
+      const double t = dispatch_makespan(units, G);
+      const bool better = !have || (c == best_c ? t < best_t * 0.995 : t < best_t * 0.98);
+      if (better) {
+        best_t = t;
+        best_k = k;
+        best_c = static_cast<int>(c);
+        have = true;
+      }
     }
   }
-  return best;
+  k_out = best_k;
+  c_out = best_c;
 }
 
-// Launch plan of a one-group launch: key-range parts per single-tile last
-// block (k, as choose_tail_split) and how many of the last whole blocks run
-// as two single-tile units each (c). When the whole blocks do not fill the
-// last wave (n mod SMs of them left over), those few blocks would otherwise
-// run alone on as many SMs while the rest idle; as single-tile units (1.33x
-// the cost per tile, half the length) they spread over every SM. The same
-// dispatch simulation as choose_tail_split decides, for c in {0, that
-// remainder}; the result is kept per session for the shape it was made for.
-// The plan itself, from the launch's numbers alone.
+// The plan of one query group, from the launch's numbers alone: the same
+// choice as choose_batch_plan for a batch of one.
 void plan_units(int H, int64_t lq, int64_t tiles, bool has_ws, int forced, int G, int& k_out, int& c_out) {
   const int64_t rem = lq % 256;
   const bool single = rem > 0 && rem <= 128;
@@ -370,33 +432,19 @@ void plan_units(int H, int64_t lq, int64_t tiles, bool has_ws, int forced, int G
     k_lo = forced > 0 ? std::max(1, std::min(forced, cap)) : 1;
     k_hi = forced > 0 ? k_lo : cap;
   }
-  const int64_t left = whole % G;
-  const double full_cost = static_cast<double>(tiles);
-  const double single_cost = std::ceil(tiles / 2.0) * 1.33 + 0.5;
+  const int64_t left = sparse_last_wave(whole, G);
+  const double t_full = static_cast<double>(tiles);
   int best_k = k_lo, best_c = 0;
   double best_t = 0;
   bool have = false;
+  std::vector<double> units;
   for (int64_t c : {int64_t(0), left}) {
     if (have && c == 0) break;   // left == 0: nothing to convert
     for (int k = k_lo; k <= k_hi; ++k) {
-      std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-      for (int g = 0; g < G; ++g) free_at.push(0.0);
-      auto run = [&](double cost) {
-        const double t0 = free_at.top();
-        free_at.pop();
-        free_at.push(t0 + cost);
-      };
-      for (int64_t u = 0; u < whole - c; ++u) run(full_cost);
-      for (int64_t u = 0; u < 2 * c; ++u) run(single_cost);
-      if (single) {
-        const double part = std::ceil(std::ceil(tiles / static_cast<double>(k)) / 2.0) * 1.33 + 0.5 + (k > 1 ? 0.5 : 0.0);
-        for (int64_t u = 0; u < static_cast<int64_t>(H) * k; ++u) run(part);
-      }
-      double t = 0;
-      while (!free_at.empty()) {
-        t = std::max(t, free_at.top());
-        free_at.pop();
-      }
+      units.assign(static_cast<size_t>(whole - c), t_full);
+      units.insert(units.end(), static_cast<size_t>(2 * c), single_tile_cost(t_full));
+      if (single) units.insert(units.end(), static_cast<size_t>(H) * k, part_cost(t_full, k));
+      const double t = dispatch_makespan(units, G);
       // more parts or a conversion must gain clearly: each part and unit costs set-up
       const bool better = !have || (c == best_c ? t < best_t * 0.995 : t < best_t * 0.98);
       if (better) {
@@ -411,6 +459,8 @@ void plan_units(int H, int64_t lq, int64_t tiles, bool has_ws, int forced, int G
   c_out = best_c;
 }
 
+// The plan of a one-group launch, kept per session for the shape it was
+// made for (the simulation runs once per shape, not once per call).
 void choose_plan(sr_session* s, const ChunkView& view, int& k_out, int& c_out) {
   const int G = sr::sm_count();
   const int64_t tiles = key_tiles(s, view);
@@ -460,7 +510,7 @@ sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, con
   AttnParams<1> p;                                  // on the stack: nothing is allocated
   std::memset(&p, 0, sizeof(p));
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
-  if (!encode_rows(&p.qmap, q, s->lq, row_elems)) return SR_ERR_CUDA;
+  if (!encode_cached(s, &p.qmap, q, s->lq, row_elems)) return SR_ERR_CUDA;
   // the scratch stands in for the session's workspace for this call only
   void* own = s->buf.workspace;
   s->buf.workspace = scratch;
@@ -714,7 +764,7 @@ static sr_status attention_view(sr_session* s, const ChunkView& view, int32_t st
   std::memset(p, 0, sizeof(*p));
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
   sr_status st = SR_OK;
-  if (!encode_rows(&p->qmap, q, view.lq, row_elems)) st = SR_ERR_CUDA;
+  if (!encode_cached(s, &p->qmap, q, view.lq, row_elems)) st = SR_ERR_CUDA;
   if (st == SR_OK) st = fill_session(p->sess[0], s, view, step, k, v, 0);
   int n_units = 0;
   if (st == SR_OK) {
@@ -812,7 +862,7 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
   if (!p) return SR_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   sr_status st = SR_OK;
-  if (!encode_rows(&p->qmap, q, P + M, row_elems)) st = SR_ERR_CUDA;
+  if (!encode_cached(s, &p->qmap, q, P + M, row_elems)) st = SR_ERR_CUDA;
   // Two query groups in one launch. Moving rows (longest key range first):
   // the bank of the step and the moving rows themselves. Prefix rows: the
   // bank alone -- the asymmetric mask as a choice of key set.
@@ -823,8 +873,8 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
   const Segment prefix[sr::kSegs] = {{bk, bv, s->cfg.n_sink}, {nullptr, nullptr, 0}, {nullptr, nullptr, 0},
                                      {nullptr, nullptr, 0}};
   int n = 0, full = 0, tails = 0;
-  if (st == SR_OK) st = encode_group(p->sess[n++], moving, row_elems, P, M);
-  if (st == SR_OK && P > 0) st = encode_group(p->sess[n++], prefix, row_elems, 0, P);
+  if (st == SR_OK) st = encode_group(p->sess[n++], moving, row_elems, P, M, s);
+  if (st == SR_OK && P > 0) st = encode_group(p->sess[n++], prefix, row_elems, 0, P, s);
   if (st == SR_OK) {
     for (int i = 0; i < n; ++i) place_units(p->sess[i], s->cfg.n_heads, full, tails);
     p->n_full_units = full;
@@ -893,7 +943,7 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
   std::memset(p, 0, sizeof(*p));
   const int64_t row_elems = static_cast<int64_t>(s0->cfg.n_heads) * s0->cfg.head_dim;
   sr_status st = SR_OK;
-  if (!encode_rows(&p->qmap, q, total, row_elems)) st = SR_ERR_CUDA;
+  if (!encode_cached(sessions[order[0]], &p->qmap, q, total, row_elems)) st = SR_ERR_CUDA;
   // units: every session's whole 256-row blocks (sessions by decreasing key
   // count), then the single-tile last blocks -- longest work first
   int full = 0, tails = 0;
@@ -902,10 +952,12 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
     st = fill_session(p->sess[r], sessions[i], views[i], step, k, v, q_off[i]);
     if (st == SR_OK) place_units(p->sess[r], s0->cfg.n_heads, full, tails);
   }
-  const int split = st == SR_OK ? choose_tail_split(sessions, views, order, n) : 1;
-  const int units = full + tails * split;
+  int split = 1, conv = 0;
+  if (st == SR_OK) choose_batch_plan(sessions, views, order, n, split, conv);
+  const int units = full + conv + tails * split;
   if (st == SR_OK) {
     p->n_full_units = full;
+    p->n_conv = conv;
     p->tail_split = split;
     p->n_sess = n;
     p->n_heads = s0->cfg.n_heads;

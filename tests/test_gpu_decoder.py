@@ -55,3 +55,35 @@ def test_decoder_layer_stream(gh, gw, H, d, shifted):
         assert_attention_close(got, ref.reshape(-1, H, d), f"chunk {c} (cache {min(2 * c, 4)} frames)")
     assert lay.error_status() == 0
     lay.close()
+
+
+def test_decoder_layer_graph_replay_matches_eager():
+    """A layer's launches captured in a CUDA graph (persistent launches whose
+    work counter the last CTA clears) replay to the eager result, bit for bit:
+    the unit order changes nothing in the arithmetic."""
+    from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
+    dev = device()
+    H, d, G = 4, 128, 5
+    for shifted in (False, True):
+        lay = DecoderWindowLayer(45, 80, H, d, G, shifted=shifted, device=dev)
+        rng = np.random.default_rng(7 + shifted)
+        mk = lambda: _bits_dev(syn.normal_bf16_bits((lay.rows, H, d), rng), dev)
+        q, k, v, ck, cv = mk(), mk(), mk(), mk(), mk()
+        lay.set_global(_bits_dev(syn.normal_bf16_bits((G, H, d), rng), dev),
+                       _bits_dev(syn.normal_bf16_bits((G, H, d), rng), dev))
+        for _ in range(2):
+            lay.commit(ck, cv)
+        o = torch.empty_like(q)
+        lay.attention(q, k, v, out=o)
+        torch.cuda.synchronize()
+        want = o.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            lay.attention(q, k, v, out=o)
+        for _ in range(3):
+            o.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(o, want)
+        assert lay.error_status() == 0
+        lay.close()

@@ -95,8 +95,9 @@ def _plan_model(H, lq, tiles, ws, forced, sms):
     if single and ws:
         cap = min(4, tiles)
         ks = [max(1, min(forced, cap))] if forced else list(range(1, cap + 1))
+    left = whole % sms if whole >= sms and whole % sms <= sms // 2 else 0
     best = None
-    for c in ([0, whole % sms] if whole % sms else [0]):
+    for c in ([0, left] if left else [0]):
         for k in ks:
             costs = [float(tiles)] * (whole - c) + [math.ceil(tiles / 2) * 1.33 + 0.5] * (2 * c)
             if single:
