@@ -71,7 +71,7 @@ struct alignas(128) AttnParams {
   int32_t n_full_units;           // whole 256-row blocks (all sessions); last blocks follow
   int32_t n_conv;                 // the last n_conv whole blocks each run as two single-tile units,
                                   // which balance the end of the launch
-  int32_t tail_split;             // CTAs per last block (1: no key split)
+  int32_t tail_split;             // key-range parts per single-tile last block (1: no key split)
   int32_t n_heads;
   float scale_log2;               // softmax scale * log2(e)
   int32_t lse_ld;                 // row stride of lse ([H][lse_ld]); 0 when lse is NULL

@@ -1,8 +1,9 @@
 // sr_noalloc.cu -- chunk attention for callers that cannot allocate device memory.
 //
 // sr_chunk_attention can split the key range of a chunk's last query block
-// over several CTAs; those CTAs exchange partial results through a scratch
-// area, normally the session's caller-owned workspace. Some callers cannot
+// into several work units, which exchange partial results through a scratch
+// area, and runs persistent CTAs that take units from a counter there; the
+// scratch is normally the session's caller-owned workspace. Some callers cannot
 // provide one: code that runs where cudaMalloc is off limits (inside a
 // framework's memory pool with a fixed budget, in a plugin that must not touch
 // the allocator, or in a process that only receives a stream and a few

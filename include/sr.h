@@ -83,8 +83,8 @@ typedef struct {
   float rope_base;          /* rotary base (e.g. 10000); > 1 */
   float softmax_scale;      /* <= 0 selects 1/sqrt(head_dim) */
   uint64_t wait_timeout_ns; /* bound on every device-side wait; 0 selects 2 s */
-  int32_t tail_split;       /* key-range split of a chunk's last, single-tile query block across
-                               CTAs: 0 = chosen per call, 1 = never, 2..4 = exactly that many
+  int32_t tail_split;       /* key-range split of a chunk's last, single-tile query block into
+                               work units: 0 = chosen per call, 1 = never, 2..4 = exactly that many
                                (needs a workspace; clamped to the number of key tiles) */
 } sr_config;
 
@@ -174,8 +174,8 @@ SR_API sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream);
  * lse: optional [H][F*T] fp32 natural-log sum-exp of the scaled scores (NULL to skip).
  * bf16 operands, fp32 accumulation and fp32 online softmax on the tensor cores.
  * When the chunk's last 256-row query block holds a single 128-row tile and the
- * session has a workspace, that block's key range may be split over several CTAs
- * (sr_config.tail_split); the last CTA to finish merges the partial results. With a
+ * session has a workspace, that block's key range may be split over several work units
+ * (sr_config.tail_split); the last part to finish merges the partial results. With a
  * workspace the launch is persistent (one CTA per SM taking work units from a counter
  * in the workspace). Calls of one session that overlap on the GPU race on that
  * workspace. After a device timeout (err_word set) initialise the session again: a
