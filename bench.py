@@ -255,6 +255,7 @@ def run_ours(args):
                    "lk": shape.lk(full), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: two ~280 MB sessions used alternately"},
         "attention_ms_per_denoise_step": round(attn_avg, 4),
+        "attention_ms_p10_p50_p90": [round(float(np.percentile(attn_ms, q)), 4) for q in (10, 50, 90)],
         "attention_tflops": round(achieved, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4), "traffic": traffic,
@@ -842,6 +843,159 @@ def run_decoder(args):
     print(json.dumps(out), flush=True)
 
 
+def run_batch(args):
+    """The multi-session serving batch: 8 independent 832x480 sessions whose
+    rings hold 0, 1, 2, 3, 4, 5, 6 and 6 frames (ragged key lengths), their
+    chunks packed along the rows and attended in one launch per denoising
+    step. Reports aggregate TFLOP/s of the batched step and each session's
+    step run alone, for comparison."""
+    import chunked_kv_cache_gb300 as sr
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_kv_cache_gb300 import build
+    build.build()
+    base = syn.SHAPES[2]
+    T, H, d, S, W, F = base.tokens_per_frame, base.n_heads, base.head_dim, base.n_sink, base.window_frames, \
+        base.chunk_frames
+    fills = [0, 1, 2, 3, 4, 5, 6, 6]
+    sessions = []
+    for sid, fill in enumerate(fills):
+        sink = lambda tid: syn.device_normal_bf16((base.n_steps, S, H, d), dev, 9, sid, 0, 0, tid)
+        s = sr.Session(H, d, base.grid_h, base.grid_w, F, W, S, base.n_steps, sink_k=sink(syn.T_SINK_K),
+                       sink_v=sink(syn.T_SINK_V), device=dev)
+        if fill:
+            s.ring_k.copy_(syn.device_normal_bf16((W * T, H, d), dev, 9, sid, 1, 0, syn.T_K))
+            s.ring_v.copy_(syn.device_normal_bf16((W * T, H, d), dev, 9, sid, 1, 0, syn.T_V))
+            s.slot_frame.copy_(torch.tensor([f if f < fill else -1 for f in range(W)], dtype=torch.int32))
+            s.restore(fill)
+        sessions.append(s)
+    rows = F * T * len(fills)
+    mk = lambda tid: syn.device_normal_bf16((rows, H, d), dev, 9, 99, 2, 0, tid)
+    q, k, v = mk(syn.T_Q), mk(syn.T_K), mk(syn.T_V)
+    o = torch.empty_like(q)
+    lq = F * T
+
+    def timed(fn, reps):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    with Clocks(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        batch_ms = timed(lambda: sr.chunk_attention_batch(sessions, 0, q, k, v, out=o), args.steps)
+    alone = []
+    for i, s in enumerate(sessions):
+        sl = slice(i * lq, (i + 1) * lq)
+        alone.append(timed(lambda: s.chunk_attention(0, q[sl], k[sl], v[sl], out=o[sl]), max(5, args.steps // 3)))
+    for s in sessions:
+        if s.error_status() != 0:
+            raise RuntimeError("device error word set during the bench")
+    lks = [S + f * T + lq for f in fills]
+    fl = sum(4.0 * H * lq * lk * d for lk in lks)
+    achieved = fl / (batch_ms / 1e3) / 1e12
+    peak_tf, _, peak_kind = _peaks()
+    rate, done, used = _oracle_attention_rate([(lq, lk) for lk in lks], d)
+    out = {
+        "metric": "multi-session batch: chunk-attention TFLOP/s of one batched step on 1 GB300", "value": round(achieved, 2),
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "8 independent 832x480 sessions (24x128, 30x52 grid, S=2072, W=6) with ring fills "
+                               "0,1,2,3,4,5,6,6 frames, chunks packed along the rows, one launch per denoising step",
+                   "lq_total": rows, "lk": lks},
+        "batch_ms_per_step": round(batch_ms, 4),
+        "alone_ms_per_step": [round(x, 4) for x in alone],
+        "alone_sum_ms": round(sum(alone), 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4), "kernel": "attn_kernel<128,16> (sr_chunk_attention_batch)",
+                     "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "cpu_baseline": _oracle_line(rate, done, used, "one denoising step of each session, in turn"),
+        "clocks": clk.summary(),
+        "gpu_launches": (args.steps + max(args.warmup, 3)) + len(fills) * (max(5, args.steps // 3) + max(args.warmup, 3)),
+    }
+    print(json.dumps(out), flush=True)
+
+
+def run_long(args):
+    """A long session at the 832x480 shape: 240 consecutive chunks from an empty
+    ring (2 x (RoPE + attention) + commit each), the ring filling and then
+    evicting. Reports the steady-state chunk time (chunks from W/F on) and
+    checks the slot table against its closed form at the end."""
+    import chunked_kv_cache_gb300 as sr
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from chunked_kv_cache_gb300 import build
+    build.build()
+    base = syn.SHAPES[2]
+    T, H, d, S, W, F = base.tokens_per_frame, base.n_heads, base.head_dim, base.n_sink, base.window_frames, \
+        base.chunk_frames
+    n_chunks = 240
+    sink = lambda tid: syn.device_normal_bf16((base.n_steps, S, H, d), dev, 10, 0, 0, 0, tid)
+    s = sr.Session(H, d, base.grid_h, base.grid_w, F, W, S, base.n_steps, sink_k=sink(syn.T_SINK_K),
+                   sink_v=sink(syn.T_SINK_V), device=dev)
+    xs = [syn.chunk_inputs_device(base, 10, dev, chunk=c) for c in range(4)]   # rotated through the stream
+    o = torch.empty_like(xs[0]["q"][0])
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [mk() for _ in range(n_chunks)]
+    with Clocks(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        for c in range(n_chunks):
+            x = xs[c % len(xs)]
+            evs[c][0].record()
+            for st in range(base.n_steps):
+                s.rope3d_qk(x["q"][st], x["k"][st])
+                s.chunk_attention(st, x["q"][st], x["k"][st], x["v"][st], out=o)
+            s.cache_commit(x["clean_k"], x["clean_v"])
+            evs[c][1].record()
+        torch.cuda.synchronize()
+    if s.error_status() != 0:
+        raise RuntimeError("device error word set during the bench")
+    n = s.frames
+    want = [max((g for g in range(n) if g % W == slot), default=-1) for slot in range(W)]
+    slots_ok = s.slot_frame.cpu().tolist() == want and n == n_chunks * F
+    ms = [a.elapsed_time(b) for a, b in evs]
+    first_full = (W + F - 1) // F
+    steady = ms[first_full:]
+    lk_full = S + W * T + F * T
+    fl_chunk = base.n_steps * 4.0 * H * F * T * lk_full * d
+    steady_ms = statistics.median(steady)
+    peak_tf, _, peak_kind = _peaks()
+    achieved = fl_chunk / (steady_ms / 1e3) / 1e12
+    rate, done, used = _oracle_attention_rate([(F * T, lk_full)], d)
+    out = {
+        "metric": "long session: steady-state ms per chunk over 240 chunks on 1 GB300", "value": round(steady_ms, 4),
+        "unit": "ms/chunk", "n_gpus": 1, "steps": n_chunks, "warmup": 0, "higher_is_better": False,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "832x480 session (24x128, 30x52 grid, S=2072, W=6), 240 consecutive chunks from an "
+                               "empty ring, one chunk = 2 x (RoPE-3D + chunk attention) + ring commit"},
+        "first_chunks_ms": [round(x, 4) for x in ms[:first_full + 1]],
+        "steady_ms_p10_p50_p90": [round(float(np.percentile(steady, q)), 4) for q in (10, 50, 90)],
+        "all_chunks_mean_ms": round(statistics.mean(ms), 4),
+        "slot_table_closed_form": slots_ok,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4), "what": "whole chunk (attention FLOPs) in steady state",
+                     "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "cpu_baseline": _oracle_line(rate, done, used, f"one steady-state denoising step ({F * T} queries x "
+                                     f"{lk_full} keys); ms per chunk extrapolated to all heads and both steps",
+                                     value=round(fl_chunk / rate * 1e3, 1), unit="ms/chunk"),
+        "clocks": clk.summary(),
+        "gpu_launches": 5 * n_chunks,
+    }
+    if not slots_ok:
+        raise RuntimeError("slot table does not match its closed form")
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -849,11 +1003,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, choices=[2, 3], default=2)
-    ap.add_argument("--workload", choices=["steady", "rhythm", "window", "graph", "decoder"], default="steady",
+    ap.add_argument("--workload", choices=["steady", "rhythm", "window", "graph", "decoder", "batch", "long"],
+                    default="steady",
                     help="steady: the headline chunk workload; rhythm: the pages' 3/2-latent unit rhythm; "
                          "window: the page-faithful window (recomputed history rows as queries); "
                          "graph: eager calls vs CUDA-graph replay of a chunk; decoder: the streaming decoder's "
-                         "window attention")
+                         "window attention; batch: 8 ragged 832x480 sessions in one launch; long: 240 chunks of "
+                         "one 832x480 session from an empty ring")
     ap.add_argument("--profile", action="store_true",
                     help="under a profiler: skip the end-to-end and CPU-baseline legs (their numbers are not reported)")
     args = ap.parse_args()
@@ -869,6 +1025,10 @@ def main():
         run_graph(args)
     elif args.workload == "decoder":
         run_decoder(args)
+    elif args.workload == "batch":
+        run_batch(args)
+    elif args.workload == "long":
+        run_long(args)
     else:
         run_ours(args)
 
