@@ -153,10 +153,6 @@ struct Walk {
   __device__ __forceinline__ int iters() const { return split ? h : n; }
 };
 
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 template <int NSESS>
 __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, int H, int& si, int& head,
                                             int& qb, int& part, int& tile) {
