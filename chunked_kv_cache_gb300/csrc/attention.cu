@@ -133,6 +133,8 @@ struct SmemBars {
   uint64_t x_empty;       // split mode: group 0 has read them and both O accumulators
   uint64_t part_done;     // key split: group 0's partial rows are published
   uint64_t part_last;     // key split: `last` is set
+  uint64_t o_staged[2];   // group t's rows of one O atom are in its staging buffer
+  uint64_t o_free[2];     // group t's staging buffer has been read by its tile store
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -258,10 +260,13 @@ __device__ __forceinline__ Walk unit_walk(const UnitRec& r) {
 // early. The last CTA to run out of units clears it (and the count of CTAs
 // that ran out), so that a replay of the same launch starts from zero.
 template <int NSESS>
-__device__ __forceinline__ int next_unit(const AttnParams<NSESS>& p) {
+__device__ __forceinline__ int next_unit(const AttnParams<NSESS>& p, bool& tagged) {
   if (p.unit_ctr == nullptr) return p.n_units;
   const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
-  atomicMax(p.unit_ctr, tag);
+  if (!tagged) {   // once this CTA has raised it, the counter carries this call's epoch
+    atomicMax(p.unit_ctr, tag);
+    tagged = true;
+  }
   const unsigned long long old = atomicAdd(p.unit_ctr, 1ull);
   const int u = static_cast<int>(gridDim.x + (old & 0xffffffffull));
   if (u >= p.n_units) {
@@ -310,6 +315,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     mbar_init(&bars->x_empty, BM);
     mbar_init(&bars->part_done, BM);
     mbar_init(&bars->part_last, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->o_staged[t], BM);
+      mbar_init(&bars->o_free[t], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -346,6 +355,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       auto slot_ptr = [&](int slot) -> uint8_t* {
         return slot < C::kStages ? sKV + slot * C::kTileBytes : sQ + C::kTileBytes;
       };
+      // Publish unit k's record (or the end of work) for the softmax groups.
+      // The record of the next unit goes out as soon as this unit's loads are
+      // issued, so that the softmax groups find it when they finish this
+      // unit's epilogue; its slot was last used four units back.
+      auto publish = [&](int k, int unit) {
+        UnitRec& rk = bars->rec[k % kUnitSlots];
+        if (unit >= p.n_units)
+          rk.u = -1;
+        else
+          make_unit(p, unit, rk);
+        mbar_arrive(&bars->unit_ready[k % kUnitSlots]);
+      };
+      bool tagged = false;
+      publish(0, u);
       while (ok) {
         // both Q slots (and the split-mode stage in the second) are free once
         // the previous unit's MMAs that read them are done
@@ -353,15 +376,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           ok = false;
           break;
         }
-        UnitRec& r = bars->rec[uk % kUnitSlots];
-        if (u >= p.n_units) {
-          r.u = -1;
-          mbar_arrive(&bars->unit_ready[uk % kUnitSlots]);
+        const UnitRec& r = bars->rec[uk % kUnitSlots];
+        if (r.u < 0) {
           mbar_arrive(&bars->q_full);
           break;
         }
-        make_unit(p, u, r);
-        mbar_arrive(&bars->unit_ready[uk % kUnitSlots]);
         const AttnSession& S = p.sess[r.si];
         const TileMap& tm = r.tm;
         const Walk wk = unit_walk(r);
@@ -433,8 +452,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         else
           q_shared = q;
         if (!ok) break;
+        u = next_unit(p, tagged);   // taken once this unit's loads are all issued
+        publish(uk + 1, u);
         ++uk;
-        u = next_unit(p);   // taken late, once this unit's loads are all issued
       }
       if (!ok || bars->abort) {
         // let every copy this CTA started land before shared memory is released
@@ -648,6 +668,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     uint32_t od0 = 0, od1 = 0;   // o_done completions of each tile so far
     uint32_t nx = 0;             // split-mode units so far
     uint32_t nk = 0;             // key-split units so far
+    uint32_t ns = 0;             // O atoms this group has sent through its staging buffer
     while (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[uk % kUnitSlots], (uk / kUnitSlots) & 1, wc, 8));
       if (!ok) break;
@@ -763,6 +784,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         if (ok && merge) ok = wait_bounded(&bars->o_done[1], w1 & 1u, wc, 6);
         ok = __all_sync(0xffffffffu, ok);
       }
+      // A whole 128-row tile of a shared-mode unit leaves through tile stores,
+      // one 64-column atom at a time, staged in this group's half of the K/V
+      // stage that shared mode leaves unused (D = 128): coalesced and off the
+      // load/store pipe. Not when the next unit is a split-mode one, whose
+      // third stage pair lives there (its record is out long before this).
+      bool staged = false;
+      if (D == 128 && ok && !wk.split && parts == 1 && r.q_local0 + (t + 1) * BM <= S.lq) {
+        const int kn = uk + 1;
+        ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[kn % kUnitSlots], (kn / kUnitSlots) & 1, wc, 11));
+        const UnitRec& rn = bars->rec[kn % kUnitSlots];
+        staged = ok && (rn.u < 0 || rn.n_qtiles == 2);
+      }
       // one part of a key-split last block publishes fp32 rows and their log2-sum-exp
       float* pdst = parts > 1 ? S.ws_part + ((static_cast<int64_t>(head) * kMaxTailSplit + part) * BM + row) * (D + 4)
                               : nullptr;
@@ -782,8 +815,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         f1 *= inv_l;
         __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
         const uint32_t t_o1 = tmem + lane_base + 256 + 128;
+        if (staged) {
+          // [128 rows][64 cols] bf16 with the 128-byte swizzle of the tile map:
+          // 16-byte chunk j of row r at r * 128 + ((j ^ (r % 8)) * 16)
+          uint8_t* buf = sKV + 4 * C::kTileBytes + t * C::kAtomBytes;
+#pragma unroll 1
+          for (int a = 0; a < 2 && ok; ++a) {
+            // the atom's 64 columns, normalised and packed, before the buffer wait
+            uint4 pkt[8];
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              uint32_t o[32];
+              tmem_ld32(t_o + (a * 2 + c2) * 32, o);
+              tmem_wait_ld();
+              tmem_fix(o);
+              uint32_t* w = reinterpret_cast<uint32_t*>(&pkt[c2 * 4]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f0, __uint_as_float(o[2 * i + 1]) * f0);
+            }
+            if (ns > 0) ok = __all_sync(0xffffffffu, wait_bounded(&bars->o_free[t], (ns - 1) & 1u, wc, 12));
+            if (!ok) break;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + row * 128 + ((j ^ (row & 7)) * 16)) = pkt[j];
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->o_staged[t]);
+            if (row == 0) {   // the group's first thread sends the atom
+              if (wait_bounded(&bars->o_staged[t], ns & 1u, wc, 13)) {
+                tma_store_2d(&p.omap, buf, head * D + a * 64, S.q_row0 + r.q_local0 + t * BM);
+                bulk_commit_group();
+                bulk_wait_read_all();
+              }
+              mbar_arrive(&bars->o_free[t]);
+            }
+            ++ns;
+          }
+        }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
+          if (staged) break;
           uint32_t o[32];
           tmem_ld32(t_o + c * 32, o);
           tmem_wait_ld();
@@ -896,6 +966,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
   }
 
+  // shared memory outlives every tile store's read of it (the stores' writes
+  // complete with the grid)
+  if (warp < 8 && threadIdx.x % BM == 0) bulk_wait_read_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
