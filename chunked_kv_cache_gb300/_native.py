@@ -20,7 +20,7 @@ SR_ERR_STATE = -4
 SR_ERR_CUDA = -5
 SR_ERR_TIMEOUT = -6
 SR_DEVERR_WAIT_TIMEOUT = 1
-SR_MAX_BATCH = 16
+SR_MAX_BATCH = 24
 
 # every extern "C" symbol that include/sr.h declares
 EXPORTS = (

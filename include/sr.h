@@ -207,7 +207,7 @@ SR_API sr_status sr_session_free(sr_session* s);
  * Each session attends over its own bank[step], its own ring and its own rows.
  * lse (optional) is [H][q_off[n]] fp32. 1 <= n <= SR_MAX_BATCH.
  */
-#define SR_MAX_BATCH 16
+#define SR_MAX_BATCH 24
 SR_API sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32_t step,
                                    const void* q, const void* k, const void* v,
                                    const int64_t* q_off, void* o, float* lse, void* stream);
