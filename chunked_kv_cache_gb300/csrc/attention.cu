@@ -43,7 +43,10 @@
 // Issue order of the MMA thread, i = iteration:
 //   S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 PV1_1 S1_2 | ...
 // so while softmax group 0 works on S0_i the tensor pipe runs PV1_{i-1} and
-// S1_i, and the other way round. Online softmax in fp32 with exp2 and the
+// S1_i, and the other way round. A softmax group hands its P over in two
+// parts: the PV MMAs over the first keys start while it still converts the
+// rest, and only the remainder of PV sits between its last P store and its
+// next S. Online softmax in fp32 with exp2 and the
 // scale folded into one packed FMA; the running maximum is only raised (and O
 // rescaled in TMEM) when a new tile exceeds it by more than 2^8, which keeps
 // numerator and denominator consistent and avoids most rescales.
@@ -69,6 +72,9 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kAttnThreads * kLaunc
               "register split exceeds what the block is launched with");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// P is handed to the PV MMAs in two parts: the first kPLoChunks 32-key chunks
+// (p_half), then the rest (p_full).
+constexpr int kPLoChunks = 2;
 
 template <int D>
 struct Cfg {
@@ -126,6 +132,7 @@ struct SmemBars {
   uint64_t kv_full[8];    // shared-mode pairs at [0, kPairs), split-mode pairs at [4, 4 + kPairsSplit)
   uint64_t kv_empty[8];
   uint64_t s_full[2];
+  uint64_t p_half[2];     // group t has stored the first kPLoChunks chunks of P_t
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t unit_ready[kUnitSlots];
@@ -307,6 +314,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_half[t], BM);
       mbar_init(&bars->p_full[t], BM);
       mbar_init(&bars->o_done[t], 1);
     }
@@ -507,9 +515,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           }
           return p0;
         };
-        auto wait_p = [&](int t, int it) {   // softmax group t has written P_t of iteration it
+        // softmax group t has written the first part (half) or all of P_t of iteration it
+        auto wait_p = [&](int t, int it, bool half) {
           const uint32_t par = ((t == 0 ? pb0 : pb1) + static_cast<uint32_t>(it)) & 1u;
-          if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->p_full[t], par, wc, 4));
+          if (ok) ok = __all_sync(0xffffffffu, wait_bounded(half ? &bars->p_half[t] : &bars->p_full[t], par, wc,
+                                                            half ? 14 : 4));
           tc_fence_after();
         };
         auto qk = [&](int t, int stage) {   // S_t = Q_t K^T
@@ -523,14 +533,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             mma_ss_w(d_tmem, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u, leader);
           }
         };
-        auto pv = [&](int t, int stage, bool acc) {   // O_t += P_t V
+        // O_t += P_t V over key steps [k0, k1) of 16 keys
+        auto pv_part = [&](int t, int stage, bool acc, int k0, int k1) {
           const uint32_t d_tmem = tmem + 256 + t * 128;
           const uint32_t a_tmem = tmem + t * BN;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
+          for (int kk = k0; kk < k1; ++kk) {
             const uint64_t bd = sdesc_sw128(stage_addr(stage) + kk * 16 * 128, C::kAtomBytes, 1024);
             mma_ts_w(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u, leader);
           }
+        };
+        // O_t += P_t V of iteration it, each part of P as soon as it is stored
+        auto pv = [&](int t, int stage, bool acc, int it) {
+          wait_p(t, it, true);
+          if (!ok) return;
+          pv_part(t, stage, acc, 0, 2 * kPLoChunks);
+          wait_p(t, it, false);
+          if (!ok) return;
+          pv_part(t, stage, acc, 2 * kPLoChunks, BN / 16);
         };
         if (!wk.split) {
           // Shared mode: both tiles walk all n key tiles, and the loop carries
@@ -559,14 +579,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           for (int i = 1; i < n && ok; ++i) {
             const int pi = take();
             tc_fence_after();
-            wait_p(0, i - 1);
+            pv(0, 2 * pi + 1, i > 1, i - 1);
             if (!ok) break;
-            pv(0, 2 * pi + 1, i > 1);
             qk(0, 2 * pi);
             tc_commit_w(&bars->s_full[0], leader);
-            wait_p(1, i - 1);
+            pv(1, 2 * pi + 1, i > 1, i - 1);
             if (!ok) break;
-            pv(1, 2 * pi + 1, i > 1);
             qk(1, 2 * pi);
             tc_commit_w(&bars->s_full[1], leader);
             tc_commit_w(&bars->kv_empty[bar0 + pi], leader);
@@ -577,14 +595,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           if (ok) {
             const int pl = take();
             tc_fence_after();
-            wait_p(0, n - 1);
+            if (ok) pv(0, 2 * pl + 1, n > 1, n - 1);
             if (ok) {
-              pv(0, 2 * pl + 1, n > 1);
               tc_commit_w(&bars->o_done[0], leader);
-              wait_p(1, n - 1);
+              pv(1, 2 * pl + 1, n > 1, n - 1);
             }
             if (ok) {
-              pv(1, 2 * pl + 1, n > 1);
               tc_commit_w(&bars->o_done[1], leader);
               tc_commit_w(&bars->kv_empty[bar0 + pl], leader);
             }
@@ -602,9 +618,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
               if (!ok) break;
               tc_fence_after();
               if (p0) {
-                wait_p(0, i - 1);
+                pv(0, 2 * pr + 1, i > 1, i - 1);
                 if (!ok) break;
-                pv(0, 2 * pr + 1, i > 1);
                 if (i == c0) tc_commit_w(&bars->o_done[0], leader);
               }
               if (q0) {
@@ -620,9 +635,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
               if (!ok) break;
               tc_fence_after();
               if (p1) {
-                wait_p(1, i - 1);
+                pv(1, 2 * pr + 1, i > 1, i - 1);
                 if (!ok) break;
-                pv(1, 2 * pr + 1, i > 1);
                 if (i == c1) tc_commit_w(&bars->o_done[1], leader);
               }
               if (q1) {
@@ -735,24 +749,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             pk[k] = pack_bf16x2(e.x, e.y);
           }
           tmem_st16(t_s + c * 16, pk);
+          if (c == kPLoChunks - 1) {
+            if (rescale && j > 0) {
+              // O was last written by PV_{j-1}, which completed before S_j was
+              // signalled (in-order tensor pipe; a commit covers all prior
+              // MMAs); no MMA of PV_j is issued before this thread arrives on
+              // p_half. Done here, where the scores of the chunks already
+              // converted no longer hold registers.
+#pragma unroll
+              for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(t_o + q * 32, o);
+                tmem_wait_ld();
+                tmem_fix(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                tmem_st32(t_o + q * 32, o);
+              }
+            }
+            // the first part of P (and a rescaled O) is in TMEM: its PV MMAs may start
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->p_half[t]);
+          }
         }
         const float2 s01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         l = l * f + (s01.x + s01.y);
-        if (rescale && j > 0) {
-          // O was last written by PV_{j-1}, which completed before S_j was
-          // signalled (in-order tensor pipe; a commit covers all prior MMAs);
-          // PV_j is not issued before this thread arrives on p_full below.
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
-            tmem_wait_ld();
-            tmem_fix(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tmem_st32(t_o + c * 32, o);
-          }
-        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
