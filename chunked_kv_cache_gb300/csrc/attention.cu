@@ -151,6 +151,82 @@ struct SmemBars {
   UnitRec rec[kUnitSlots];
 };
 
+// The last part of a key-split last block combines every part's published
+// fp32 rows (O and the log2-sum-exp in column D of [part][128][D + 4]) into
+// bf16 output rows and their natural-log LSE. Warp w of the merging group
+// takes rows w, w + 4, ... and each lane D/32 columns of them, so that a load
+// or store of a row is one contiguous access of the warp, and the loads of all
+// parts of two rows are in flight together. Out of line: it runs once per
+// last block and keeps its registers out of the softmax loop's allocation.
+template <int D>
+__device__ __noinline__ void merge_key_parts(const float* __restrict__ hbase, int parts, int n_live,
+                                             __nv_bfloat16* __restrict__ o, int n_heads, int head, int64_t row0,
+                                             float* __restrict__ lse, int64_t lse_ld, int w, int lane) {
+  __threadfence();
+  constexpr int kCpl = D / 32;   // columns per lane
+  constexpr int kMergeRows = 4;
+  const int64_t pstride = static_cast<int64_t>(BM) * (D + 4);
+#pragma unroll 1
+  for (int rb = w; rb < n_live; rb += 4 * kMergeRows) {
+    float lw[kMergeRows][kMaxTailSplit];
+    float x[kMergeRows][kMaxTailSplit][kCpl];
+#pragma unroll
+    for (int q = 0; q < kMergeRows; ++q) {
+      const int rr = min(rb + 4 * q, n_live - 1);   // a row past the end repeats the last one
+#pragma unroll
+      for (int k = 0; k < kMaxTailSplit; ++k) {
+        lw[q][k] = -INFINITY;
+        if (k < parts) {
+          const float* src = hbase + k * pstride + static_cast<int64_t>(rr) * (D + 4);
+          lw[q][k] = __ldcg(src + D);
+          if constexpr (kCpl == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+            x[q][k][0] = v.x; x[q][k][1] = v.y; x[q][k][2] = v.z; x[q][k][3] = v.w;
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(src) + lane);
+            x[q][k][0] = v.x; x[q][k][1] = v.y;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kCpl; ++c) x[q][k][c] = 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kMergeRows; ++q) {
+      const int rr = rb + 4 * q;
+      if (rr < n_live) {
+        float mx = lw[q][0];
+#pragma unroll
+        for (int k = 1; k < kMaxTailSplit; ++k) mx = fmaxf(mx, lw[q][k]);
+        float L = 0.f;
+        float a[kCpl];
+#pragma unroll
+        for (int c = 0; c < kCpl; ++c) a[c] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxTailSplit; ++k) {
+          const float wk = ex2_approx(lw[q][k] - mx);   // 0 for an absent part
+          L += wk;
+#pragma unroll
+          for (int c = 0; c < kCpl; ++c) a[c] = fmaf(wk, x[q][k][c], a[c]);
+        }
+        const float invL = 1.f / L;
+        __nv_bfloat16* dst = o + ((row0 + rr) * n_heads + head) * D + lane * kCpl;
+        if constexpr (kCpl == 4) {
+          uint2 pk;
+          pk.x = pack_bf16x2(a[0] * invL, a[1] * invL);
+          pk.y = pack_bf16x2(a[2] * invL, a[3] * invL);
+          *reinterpret_cast<uint2*>(dst) = pk;
+        } else {
+          *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(a[0] * invL, a[1] * invL);
+        }
+        if (lane == 0 && lse != nullptr)
+          lse[static_cast<int64_t>(head) * lse_ld + row0 + rr] = (mx + __log2f(L)) * 0.69314718055994531f;
+      }
+    }
+  }
+}
+
 // The key tiles each query tile walks, within the unit's range [lo, lo + n) of
 // all key tiles: in shared mode both walk the whole range; in split mode tile 0
 // walks [lo, lo + h) and tile 1 walks [lo + h, lo + n).
@@ -946,43 +1022,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         }
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->part_last, nk & 1u, wc, 10));
         ++nk;
-        if (ok && bars->last && live) {
-          __threadfence();
-          const float* base = S.ws_part + (static_cast<int64_t>(head) * kMaxTailSplit * BM + row) * (D + 4);
-          const int64_t pstride = static_cast<int64_t>(BM) * (D + 4);
-          float w[kMaxTailSplit];
-          float mx = -INFINITY;
-          for (int k = 0; k < parts; ++k) {
-            w[k] = __ldcg(base + k * pstride + D);
-            mx = fmaxf(mx, w[k]);
-          }
-          float L = 0.f;
-          for (int k = 0; k < parts; ++k) {
-            w[k] = ex2_approx(w[k] - mx);
-            L += w[k];
-          }
-          const float invL = 1.f / L;
-          for (int k = 0; k < parts; ++k) w[k] *= invL;
-          __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
-#pragma unroll 1
-          for (int c = 0; c < D; c += 8) {
-            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < parts; ++k) {
-              const float4 x0 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c));
-              const float4 x1 = __ldcg(reinterpret_cast<const float4*>(base + k * pstride + c + 4));
-              a[0] += w[k] * x0.x; a[1] += w[k] * x0.y; a[2] += w[k] * x0.z; a[3] += w[k] * x0.w;
-              a[4] += w[k] * x1.x; a[5] += w[k] * x1.y; a[6] += w[k] * x1.z; a[7] += w[k] * x1.w;
-            }
-            uint4 pkt;
-            pkt.x = pack_bf16x2(a[0], a[1]);
-            pkt.y = pack_bf16x2(a[2], a[3]);
-            pkt.z = pack_bf16x2(a[4], a[5]);
-            pkt.w = pack_bf16x2(a[6], a[7]);
-            *reinterpret_cast<uint4*>(dst + c) = pkt;
-          }
-          if (p.lse != nullptr)
-            p.lse[static_cast<int64_t>(head) * p.lse_ld + out_row] = (mx + __log2f(L)) * 0.69314718055994531f;
-        }
+        if (ok && bars->last)
+          merge_key_parts<D>(S.ws_part + static_cast<int64_t>(head) * kMaxTailSplit * BM * (D + 4), parts,
+                             min(BM, S.lq - r.q_local0), p.o, p.n_heads, head,
+                             static_cast<int64_t>(S.q_row0) + r.q_local0, p.lse, p.lse_ld, warp % 4, lane);
       }
       ++uk;
     }
