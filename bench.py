@@ -47,6 +47,12 @@ METRIC = "chunk-attention ms/step and TFLOP/s on 1 GB300; % of bf16 tensor peak"
 UNIT = "TFLOP/s"
 
 
+# The part's nominal dense figures, reported beside the measured peaks and
+# labelled as such: bf16 tensor throughput without sparsity, and HBM3e bandwidth.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -260,13 +266,17 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4), "traffic": traffic,
                      "kernel": "attn_kernel (sr_chunk_attention)",
-                     "peak_kind": f"{peak_kind} bf16 dense burst"},
+                     "peak_kind": f"{peak_kind} bf16 dense burst",
+                     "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4),
+                     "nominal_peak": f"{NOMINAL_BF16_TFLOPS:.0f} TFLOP/s nominal dense bf16 (spec, not measured)"},
         "kernels": {
             "commit": {"us": round(commit_avg * 1e3, 2), "GB/s": round(commit_bytes / (commit_avg / 1e3) / 1e9, 1),
-                       "frac_hbm": round(commit_bytes / (commit_avg / 1e3) / 1e9 / peak_gbs, 4)},
+                       "frac_hbm": round(commit_bytes / (commit_avg / 1e3) / 1e9 / peak_gbs, 4),
+                       "frac_hbm_nominal": round(commit_bytes / (commit_avg / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4)},
             "rope3d_qk": {"us": round(rope_avg * 1e3, 2),
                           "GB/s": round(commit_bytes / (rope_avg / 1e3) / 1e9, 1),
-                          "frac_hbm": round(commit_bytes / (rope_avg / 1e3) / 1e9 / peak_gbs, 4)},
+                          "frac_hbm": round(commit_bytes / (rope_avg / 1e3) / 1e9 / peak_gbs, 4),
+                          "frac_hbm_nominal": round(commit_bytes / (rope_avg / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4)},
         },
         "e2e": {"value": round(aggregate_throughput(e2e["chunks"] * flops_chunk, e2e["seconds"], world) / 1e12, 2),
                 "unit": UNIT,
