@@ -156,7 +156,7 @@ struct SmemBars {
 // bf16 output rows and their natural-log LSE. Warp w of the merging group
 // takes rows w, w + 4, ... and each lane D/32 columns of them, so that a load
 // or store of a row is one contiguous access of the warp, and the loads of all
-// parts of two rows are in flight together. Out of line: it runs once per
+// parts of kMergeRows rows are in flight together. Out of line: it runs once per
 // last block and keeps its registers out of the softmax loop's allocation.
 template <int D>
 __device__ __noinline__ void merge_key_parts(const float* __restrict__ hbase, int parts, int n_live,
