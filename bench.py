@@ -397,6 +397,29 @@ def _profiled_traffic(kernel, config):
     return None if e is None or e.get("stale") else e.get("bytes_per_launch")
 
 
+def _host_info():
+    """The host's CPU model (lscpu) and BLAS thread count, for the oracle lines."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        blas = [d for d in threadpool_info() if d.get("user_api") == "blas"]
+        threads = blas[0]["num_threads"] if blas else None
+    except ImportError:
+        env = [os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS")]
+        threads = next((int(v) for v in env if v), None)
+    return {"cpu_model": model,
+            "blas_threads": threads if threads is not None else f"library default ({os.cpu_count()} cores)"}
+
+
 def cpu_baseline(shape, args, budget_s: float = 12.0):
     """The float64 oracle, as it stands, on this host's cores: attention of
     whole heads of one denoising step (full window) until the time budget is
@@ -417,7 +440,7 @@ def cpu_baseline(shape, args, budget_s: float = 12.0):
     flops = 4.0 * heads_done * shape.lq * lk * shape.head_dim
     return {"value": round(flops / t_used / 1e12, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{heads_done} of {shape.n_heads} heads of one denoising step "
-                      f"({shape.lq} queries x {lk} keys, float64 numpy), {t_used:.1f} s"}
+                      f"({shape.lq} queries x {lk} keys, float64 numpy), {t_used:.1f} s", **_host_info()}
 
 
 def _oracle_attention_rate(parts, d, budget_s: float = 6.0):
@@ -443,7 +466,7 @@ def _oracle_attention_rate(parts, d, budget_s: float = 6.0):
 def _oracle_line(rate, done, used, what, value=None, unit=UNIT):
     """cpu_baseline object: TFLOP/s unless a converted value and unit are given."""
     return {"value": round(rate / 1e12, 5) if value is None else value, "unit": unit, "cores": os.cpu_count(),
-            "kind": "oracle", "sample": f"{done} heads of {what} (float64 numpy), {used:.1f} s"}
+            "kind": "oracle", "sample": f"{done} heads of {what} (float64 numpy), {used:.1f} s", **_host_info()}
 
 
 def run_reference(args):
@@ -476,7 +499,7 @@ def run_reference(args):
            "config": {"workload": shape.name + ", steady state (ring full)", "heads": shape.n_heads,
                       "lq": shape.lq, "lk": lk},
            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                            "sample": sample},
+                            "sample": sample, **_host_info()},
            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
