@@ -221,6 +221,41 @@ def test_evicted_frames_give_bit_identical_output():
     assert np.array_equal(oa, ob)
 
 
+def test_checkpoint_and_resume_continue_bit_for_bit():
+    # A session's state is its sink banks, ring, slot table and frame count. A
+    # session built from copies of them (the count through sr_session_restore)
+    # continues bit for bit: same outputs, same ring, same slot table.
+    import chunked_kv_cache_gb300 as sr
+    shape = syn.TINY
+    a = Twin(shape, 1)
+    for c in range(5):      # 10 frames through a 4-frame ring: the ring has wrapped
+        a.commit(syn.chunk_inputs(shape, 1, chunk=c))
+    g = a.gpu
+    b = sr.Session(shape.n_heads, shape.head_dim, shape.grid_h, shape.grid_w, shape.chunk_frames,
+                   shape.window_frames, shape.n_sink, shape.n_steps, sink_k=g.sink_k.clone(),
+                   sink_v=g.sink_v.clone(), device=a.dev)
+    b.ring_k.copy_(g.ring_k)
+    b.ring_v.copy_(g.ring_v)
+    b.slot_frame.copy_(g.slot_frame)
+    b.restore(g.frames)
+    assert b.frames == g.frames == 10
+    for c in range(5, 8):
+        x = syn.chunk_inputs(shape, 1, chunk=c)
+        for st in range(shape.n_steps):
+            q, k, v = to_dev(x.q[st], a.dev), to_dev(x.k[st], a.dev), to_dev(x.v[st], a.dev)
+            q2, k2 = q.clone(), k.clone()
+            g.rope3d_qk(q, k)
+            b.rope3d_qk(q2, k2)
+            assert torch.equal(g.chunk_attention(st, q, k, v), b.chunk_attention(st, q2, k2, v))
+        ck, cv = to_dev(x.clean_k, a.dev), to_dev(x.clean_v, a.dev)
+        g.cache_commit(ck, cv)
+        b.cache_commit(ck, cv)
+    assert torch.equal(g.ring_k, b.ring_k) and torch.equal(g.ring_v, b.ring_v)
+    assert torch.equal(g.slot_frame, b.slot_frame)
+    assert b.frames == g.frames == 16
+    assert g.error_status() == 0 and b.error_status() == 0
+
+
 def test_clock_shift_invariance_without_sinks():
     shape = syn.TINY
     outs = []
