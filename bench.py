@@ -154,23 +154,12 @@ def _make_session(shape, config, sess_id, dev):
     return s, x
 
 
-def _chunk(s, x, n_steps, ev=None):
+def _chunk(s, x, n_steps):
     """One streaming chunk through the library: 2 x (RoPE + attention) + commit."""
     for st in range(n_steps):
-        if ev is not None:
-            ev["rope"][0].record()
         s.rope3d_qk(x["q"][st], x["k"][st])
-        if ev is not None:
-            ev["rope"][1].record()
-            ev["attn"][0].record()
         s.chunk_attention(st, x["q"][st], x["k"][st], x["v"][st], out=x["o"][st])
-        if ev is not None:
-            ev["attn"][1].record()
-    if ev is not None:
-        ev["commit"][0].record()
     s.cache_commit(x["clean_k"], x["clean_v"])
-    if ev is not None:
-        ev["commit"][1].record()
 
 
 def run_ours(args):
