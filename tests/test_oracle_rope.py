@@ -113,3 +113,56 @@ def test_token_positions_frame_row_column():
     assert t.tolist() == [7] * 6 + [8] * 6
     assert h.tolist() == [0, 0, 0, 1, 1, 1] * 2
     assert w.tolist() == [0, 1, 2] * 4
+
+
+# --- positions far from the origin: the stream time grows without bound ---
+
+def test_two_pi_and_frequencies_closed_forms():
+    from decimal import Decimal, localcontext
+    from oracle.rope import omega, two_pi
+    assert float(two_pi() / 2) == math.pi
+    assert abs(float(two_pi()) - 2 * math.pi) == 0.0
+    # 10000 ** (-2*11/44) = 10000 ** -0.5 = 1/100 exactly; 10000 ** (-2/4) likewise
+    assert abs(omega(11, 44, 10000.0) - Decimal("0.01")) < Decimal(10) ** -55
+    assert abs(omega(1, 4, 10000.0) - Decimal("0.01")) < Decimal(10) ** -55
+    # frequencies of one axis form a geometric sequence: w_i * w_j = w_0 * w_(i+j)
+    with localcontext() as ctx:
+        ctx.prec = 80
+        assert abs(omega(3, 42, 10000.0) * omega(5, 42, 10000.0) - omega(8, 42, 10000.0)) < Decimal(10) ** -55
+    assert omega(0, 42, 10000.0) == 1
+
+
+@pytest.mark.parametrize("t", [2 ** 24 + 3, 2 ** 30, 2 ** 33, 2 ** 40, -(2 ** 40) + 7, 123456789012])
+def test_huge_time_turns_a_frequency_one_pair_by_exactly_t_radians(t):
+    # d = 6: the t axis holds a single pair with frequency base**0 = 1, so its
+    # angle is t radians; math.cos/sin of the float64 t (exact below 2**53)
+    # reduce the argument exactly.
+    x = np.array([[[0.75, -1.25, 0.0, 0.0, 0.0, 0.0]]])
+    y = rope3d(x, np.array([t]), np.array([0]), np.array([0]), 10000.0)[0, 0]
+    c, s = math.cos(float(t)), math.sin(float(t))
+    assert np.allclose(y[0:2], [0.75 * c + 1.25 * s, 0.75 * s - 1.25 * c], rtol=0, atol=4e-16)
+
+
+def test_composition_holds_at_large_positions():
+    # R(p1) R(p2) = R(p1 + p2) for every pair of a d = 128 head. A float64
+    # product p * omega would break this by ~|p| * 2**-53 rad (6e-5 at 2**39).
+    x = _x(L=3, H=2, d=128, seed=9)
+    p1 = (np.array([2 ** 39 + 5, 2 ** 33, 2 ** 24 + 1]), np.array([0, 7, 3]), np.array([1, 0, 9]))
+    p2 = (np.array([2 ** 38 - 3, 12345, 2 ** 31]), np.array([4, 0, 1]), np.array([2, 6, 0]))
+    a = rope3d(rope3d(x, *p1, 10000.0), *p2, 10000.0)
+    b = rope3d(x, *(u + v for u, v in zip(p1, p2)), 10000.0)
+    assert np.allclose(a, b, rtol=0, atol=1e-13)
+
+
+def test_scores_depend_only_on_position_difference_at_large_offsets():
+    g = np.random.default_rng(4)
+    q = g.standard_normal((1, 2, 128))
+    k = g.standard_normal((1, 2, 128))
+    pq = (np.array([4]), np.array([2]), np.array([9]))
+    pk = (np.array([1]), np.array([5]), np.array([3]))
+    s0 = np.einsum("lhd,lhd->h", rope3d(q, *pq, 10000.0), rope3d(k, *pk, 10000.0))
+    for dt in (2 ** 24 + 3, 2 ** 35 + 17, 2 ** 40):
+        sh = (pq[0] + dt, pq[1], pq[2])
+        kh = (pk[0] + dt, pk[1], pk[2])
+        s1 = np.einsum("lhd,lhd->h", rope3d(q, *sh, 10000.0), rope3d(k, *kh, 10000.0))
+        assert np.allclose(s0, s1, rtol=0, atol=1e-12)
