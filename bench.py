@@ -1,15 +1,18 @@
 """Benchmark of the streaming chunk-attention hot path on GB300.
 
-One bench step = one streaming chunk of the 832x480 workload in steady state
-(ring full): for each of the two denoising steps, RoPE-3D on the chunk's Q/K
-and the chunk attention over sink bank + 6-frame ring + chunk; then the ring
-commit. Inputs are seeded synthetic bf16 N(0,1), resident in HBM before the
-timed region. Two independent sessions (about 280 MB of buffers each) are
-used alternately, so every step reads inputs that were last touched more
-than an L2's worth of traffic ago.
+The default workload is the 720p chunk (40 heads x 128, 45x80 latent grid,
+two-frame chunks, sinks of 4112 tokens, an 8-frame ring), the largest
+configuration that fits one GPU, in steady state (ring full): per chunk, for
+each of the two denoising steps, RoPE-3D on the chunk's Q/K and the chunk
+attention over sink bank + ring + chunk; then the ring commit. A bench step is
+several chunks (8 at 720p, about 50 ms), so that the clock sampler sees the GPU
+under load throughout the timed steps. Inputs are seeded synthetic bf16 N(0,1),
+resident in HBM before the timed region. Two independent sessions are used
+alternately, so every chunk reads inputs that were last touched more than an
+L2's worth of traffic ago. ``--config 2`` runs the 832x480 chunk instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2|3]
-                    [--workload steady|rhythm|window|graph|decoder]
+                    [--workload steady|rhythm|window|graph|decoder|batch|long]
 
 ``--workload rhythm`` times the pages' unit rhythm instead (chunks of 3 and 2
 latent frames at the 832x480 frame size) and ``--workload window`` the
@@ -44,6 +47,8 @@ import torch
 import synthetic as syn
 
 METRIC = "chunk-attention ms/step and TFLOP/s on 1 GB300; % of bf16 tensor peak"
+# chunks per bench step of the steady workload, per config (about 50 ms per step)
+CHUNKS_PER_STEP = {2: 64, 3: 8}
 UNIT = "TFLOP/s"
 
 
@@ -177,8 +182,11 @@ def run_ours(args):
     flops_chunk = shape.n_steps * flops_attn
     commit_bytes = 4 * shape.lq * shape.n_heads * shape.head_dim * 2
     sessions = [_make_session(shape, args.config, i + 10 * rank, dev) for i in range(2)]
+    # A bench step is R chunks, enough for tens of milliseconds, so that the
+    # clock sampler sees the GPU under load many times over the timed steps.
+    R = args.chunks_per_step or CHUNKS_PER_STEP[args.config]
     torch.cuda.synchronize()
-    for i in range(args.warmup):
+    for i in range(args.warmup * R):
         s, x = sessions[i % 2]
         _chunk(s, x, shape.n_steps)
     torch.cuda.synchronize()
@@ -188,14 +196,15 @@ def run_ours(args):
     # needs: an event recorded between two launches sits between them in the
     # stream and can hold back the second one's early (programmatic) start. The
     # RoPE and commit kernels are timed back to back after the loop.
-    per = [[mk() for _ in range(shape.n_steps)] for _ in range(args.steps)]
+    n_chunks = args.steps * R
+    per = [[mk() for _ in range(shape.n_steps)] for _ in range(n_chunks)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with Clocks(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
         t0.record()
-        for i in range(args.steps):
+        for i in range(n_chunks):
             s, x = sessions[i % 2]
             p = per[i]
             for st in range(shape.n_steps):
@@ -227,7 +236,7 @@ def run_ours(args):
     peak_tf, peak_gbs, peak_kind = _peaks()
     attn_avg = statistics.mean(attn_ms)
     achieved = flops_attn / (attn_avg / 1e3) / 1e12
-    value = aggregate_throughput(args.steps * flops_chunk, elapsed, world) / 1e12
+    value = aggregate_throughput(n_chunks * flops_chunk, elapsed, world) / 1e12
     # The two HBM-bound kernels last ~20 us, close to the event timer's
     # granularity; time them again over 16 back-to-back launches each, cycling
     # through six input pairs of the two sessions (230 MB at 832x480, more than
@@ -239,7 +248,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": shape.name + ", steady state (ring full), one step = one chunk: "
+        "ms_per_chunk": round(elapsed / n_chunks * 1e3, 4), "chunks_per_step": R,
+        "config": {"workload": shape.name + f", steady state (ring full), one step = {R} chunks, each "
                                "2 x (RoPE-3D + chunk attention) + ring commit",
                    "heads": shape.n_heads, "head_dim": shape.head_dim, "lq": shape.lq,
                    "lk": shape.lk(full), "parallelism": f"replicas x{world}",
@@ -267,7 +277,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "cpu_baseline": cpu,
         "clocks": clocks,
-        "gpu_launches": (2 * shape.n_steps + 1) * args.steps,
+        "gpu_launches": (2 * shape.n_steps + 1) * n_chunks,
     }
     print(json.dumps(out), flush=True)
     if world > 1:
@@ -427,9 +437,12 @@ def cpu_baseline(shape, args, budget_s: float = 12.0):
         t_used += time.perf_counter() - t
         heads_done += 1
     flops = 4.0 * heads_done * shape.lq * lk * shape.head_dim
+    extra = ("" if heads_done == shape.n_heads else
+             f"; heads are independent, so the rate of the sampled heads stands for all {shape.n_heads} "
+             "(extrapolated linearly)")
     return {"value": round(flops / t_used / 1e12, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{heads_done} of {shape.n_heads} heads of one denoising step "
-                      f"({shape.lq} queries x {lk} keys, float64 numpy), {t_used:.1f} s", **_host_info()}
+                      f"({shape.lq} queries x {lk} keys, float64 numpy), {t_used:.1f} s{extra}", **_host_info()}
 
 
 def _oracle_attention_rate(parts, d, budget_s: float = 6.0):
@@ -1025,7 +1038,10 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, choices=[2, 3], default=2)
+    ap.add_argument("--config", type=int, choices=[2, 3], default=3,
+                    help="3: the 720p chunk (the largest single-GPU workload, default); 2: the 832x480 chunk")
+    ap.add_argument("--chunks-per-step", type=int, default=0,
+                    help="chunks per bench step of the steady workload (0: about 50 ms worth)")
     ap.add_argument("--workload", choices=["steady", "rhythm", "window", "graph", "decoder", "batch", "long"],
                     default="steady",
                     help="steady: the headline chunk workload; rhythm: the pages' 3/2-latent unit rhythm; "

@@ -30,7 +30,7 @@ EXPORTS = (
     "sr_chunk_attention_noalloc", "sr_plan_chunk", "sr_rope3d_qk_frames", "sr_chunk_attention_frames",
     "sr_cache_commit_frames", "sr_window_attention", "sr_rope3d_qk_at", "sr_rope3d_qk_dev",
     "sr_chunk_attention_dev", "sr_cache_commit_dev", "sr_window_count", "sr_plan_window",
-    "sr_plan_attention",
+    "sr_plan_attention", "sr_rope_angle",
 )
 
 
@@ -109,6 +109,7 @@ def lib() -> ctypes.CDLL:
                                                ctypes.POINTER(i64), vp, vp, vp]
         L.sr_plan_attention.argtypes = [i32, i64, i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                         ctypes.POINTER(i64)]
+        L.sr_rope_angle.argtypes = [ctypes.POINTER(SrConfig), i32, i64, ctypes.POINTER(ctypes.c_float)]
         L.sr_device_error_status.argtypes = [i32]
         L.sr_debug_wait_timeout.argtypes = [vp, u64, vp]
         L.sr_workspace_bytes.argtypes = [ctypes.POINTER(SrConfig), ctypes.POINTER(ctypes.c_uint64)]
@@ -258,6 +259,13 @@ def sr_chunk_attention_batch(handles, step: int, q: int, k: int, v: int, q_off, 
     offs = (ctypes.c_int64 * (n + 1))(*[int(x) for x in q_off])
     _check(lib().sr_chunk_attention_batch(arr, n, int(step), q, k, v, offs, o, lse or None, stream or None),
            "sr_chunk_attention_batch")
+
+
+def sr_rope_angle(cfg: SrConfig, pair: int, position: int) -> float:
+    """The reduced rotation angle (radians, float) the kernels apply to one pair (host arithmetic)."""
+    a = ctypes.c_float()
+    _check(lib().sr_rope_angle(ctypes.byref(cfg), int(pair), int(position), ctypes.byref(a)), "sr_rope_angle")
+    return a.value
 
 
 def sr_device_error_status(value: int) -> int:

@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsr.so")
-SOURCES = ["attention.cu", "rope_commit.cu", "sr_api.cu", "sr_noalloc.cu"]
+SOURCES = ["attention.cu", "rope_commit.cu", "rope_phase.cu", "sr_api.cu", "sr_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,7 +34,10 @@ def nvcc() -> str:
 
 
 def _flags(ptxas_verbose: bool):
+    # host code keeps IEEE semantics: no contraction of a*b + c into a fused
+    # multiply-add (the double-double arithmetic of rope_phase.cu relies on it)
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+                "-Xcompiler", "-ffp-contract=off",
                 "-I", INCLUDE, "-I", CSRC]
     if ptxas_verbose:
         f += ["-Xptxas", "-v"]

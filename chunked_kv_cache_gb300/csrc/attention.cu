@@ -1107,8 +1107,7 @@ __global__ void debug_wait_kernel(int32_t* err_word, uint64_t timeout_ns) {
 }  // namespace
 
 cudaError_t launch_debug_wait(int32_t* err_word, uint64_t timeout_ns, cudaStream_t st) {
-  debug_wait_kernel<<<1, 32, 0, st>>>(err_word, timeout_ns);
-  return cudaGetLastError();
+  return launch_plain(debug_wait_kernel, 1, 32, st, err_word, timeout_ns);
 }
 
 }  // namespace sr

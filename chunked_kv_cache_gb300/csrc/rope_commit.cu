@@ -83,16 +83,13 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, 
     }
 
     if (base == 0) {
-      // Angle = pos * inv_freq, carried as an unevaluated sum of two floats
-      // (the rounded product, its exact FMA error, and pos times the low half
-      // of inv_freq), then reduced by 2*pi written as two floats (Cody-Waite)
-      // before the fp32 sincos. A plain fp32 product would carry an absolute
-      // error proportional to the angle (1e-4 rad at t ~ 1000); this keeps it
-      // ~1e-7.
+      // The angle of each (token, pair): the pair's fixed-point turn constant
+      // times the integer position, reduced to one turn with integer
+      // arithmetic (rope_angle), then the fp32 sincos of that angle in [-pi, pi).
       for (int i = threadIdx.x; i < ntok * kPairs; i += kRopeThreads) {
         const int tok = tok_lo + i / kPairs;
         const int pr = i % kPairs;
-        const int ax = p.axis[pr];
+        const int ax = p.phase.axis[pr];
         const int in_frame = tok % p.tokens_per_frame;
         int64_t pos;
         if (ax == 0)
@@ -101,14 +98,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p, 
           pos = in_frame / p.grid_w;
         else
           pos = in_frame % p.grid_w;
-        const float fp = static_cast<float>(pos);            // exact below 2^24
-        const float hi = p.inv_freq_hi[pr];
-        const float prod = fp * hi;
-        const float err = fmaf(fp, p.inv_freq_lo[pr], fmaf(fp, hi, -prod));
-        const float k = rintf(prod * 0.159154943091895336f);
-        float r = fmaf(-k, 6.28318548202514648f, prod);       // 2*pi rounded to float
-        r = fmaf(-k, -1.74845553146951906e-7f, r);            // 2*pi minus that float
-        r += err;
+        const float r = rope_angle(p.phase.turn_hi[pr], p.phase.turn_lo[pr], pos, p.phase.rad_hi, p.phase.rad_lo);
         float sn, cs;
         sincosf(r, &sn, &cs);
         cs_table[i] = make_float2(cs, sn);
@@ -199,6 +189,9 @@ __global__ void init_ring_state_kernel(int32_t* slot_frame, int W, int32_t* err_
     for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ws_ctr[i] = 0;
   if (threadIdx.x == 0) *err_word = SR_DEVERR_NONE;
 }
+__global__ void zero_words_kernel(int32_t* words, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) words[i] = 0;
+}
 }  // namespace
 
 // Advance the device frame counter after a commit: its own launch, so that
@@ -206,23 +199,24 @@ __global__ void init_ring_state_kernel(int32_t* slot_frame, int W, int32_t* err_
 __global__ void advance_frames_kernel(int64_t* counter, int64_t add) { *counter += add; }
 
 cudaError_t launch_advance_frames(int64_t* counter, int64_t add, cudaStream_t st) {
-  advance_frames_kernel<<<1, 1, 0, st>>>(counter, add);
-  return cudaGetLastError();
+  return launch_plain(advance_frames_kernel, 1, 1, st, counter, add);
 }
 
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(bytes / 16);
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
-  copy16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint4*>(dst),
-                                                                static_cast<const uint4*>(src), n);
-  return cudaGetLastError();
+  return launch_plain(copy16_kernel, static_cast<unsigned>(blocks), 256, st, static_cast<uint4*>(dst),
+                     static_cast<const uint4*>(src), n);
 }
 
 cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, int32_t* ws_ctr, int n_ctr,
                                    cudaStream_t st) {
-  init_ring_state_kernel<<<1, 256, 0, st>>>(slot_frame, W, err_word, ws_ctr, n_ctr);
-  return cudaGetLastError();
+  return launch_plain(init_ring_state_kernel, 1, 256, st, slot_frame, W, err_word, ws_ctr, n_ctr);
+}
+
+cudaError_t launch_zero_words(int32_t* words, int n, cudaStream_t st) {
+  return launch_plain(zero_words_kernel, 1, 256, st, words, n);
 }
 
 }  // namespace sr

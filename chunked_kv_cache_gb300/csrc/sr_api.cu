@@ -36,10 +36,10 @@ struct sr_session {
   float scale;
   int64_t n_committed;
   int32_t epoch;              // attention calls so far (key-split counters)
+  bool counters_stale;        // the epoch wrapped: clear the workspace counters before the next launch
   int64_t plan_key[4];        // the launch plan last chosen (choose_plan), and what it was chosen for
   int32_t plan_split, plan_conv;
-  double inv_freq[64];
-  int8_t axis[64];
+  sr::RopePhase phase;        // per rotary pair: axis and fixed-point turn constant
   // Tensor maps encoded for this session's calls, by (address, rows): a map
   // holds only the address, extents and strides, so a buffer that comes back
   // (the banks, the ring, a caller's reused chunk buffers) reuses its map.
@@ -54,6 +54,9 @@ struct sr_session {
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// The slot table holds absolute frame indices as int32: a session commits at
+// most this many frames.
+constexpr int64_t kMaxFrames = INT32_MAX;
 constexpr int kBoxRows = 128;
 constexpr int kBoxCols = 64;
 
@@ -78,27 +81,6 @@ sr_status validate_config(const sr_config& c) {
       lq * row > limit || ring_rows * row > limit || static_cast<int64_t>(c.n_sink) * row * c.n_steps > limit)
     return SR_ERR_INVALID_ARG;
   return SR_OK;
-}
-
-// Rotary tables: pair p of the head (dims 2p, 2p+1) belongs to axis t, h or w
-// and turns by position * base^(-2i/d_axis), i its index inside the axis. The
-// head dim splits into [d_t | d_h | d_w], d_h = d_w = 2*floor(d/6).
-void build_rope_tables(sr_session* s) {
-  const int d = s->cfg.head_dim;
-  const int dh = 2 * (d / 6);
-  const int dt = d - 2 * dh;
-  const int dims[3] = {dt, dh, dh};
-  int p = 0;
-  for (int a = 0; a < 3; ++a) {
-    for (int i = 0; i < dims[a] / 2; ++i, ++p) {
-      s->axis[p] = static_cast<int8_t>(a);
-      s->inv_freq[p] = std::pow(static_cast<double>(s->cfg.rope_base), -2.0 * i / static_cast<double>(dims[a]));
-    }
-  }
-  for (; p < 64; ++p) {
-    s->axis[p] = 0;
-    s->inv_freq[p] = 0.0;
-  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -261,10 +243,29 @@ const char* bank_ptr(const void* bank, const sr_session* s, int step) {
 
 // A new epoch for this call's counters (27 bits: the key-split counter keeps
 // its arrivals in the low 4 bits of an int32; never 0, the cleared value).
+// The counters are raised to a call's epoch with atomicMax, so a count left by
+// a call that stopped early (a device timeout) under a high epoch would outlast
+// the wrap back to 1: after a wrap the counters are cleared on the stream
+// before the next launch (clear_stale_counters).
 int32_t next_epoch(sr_session* s) {
   s->epoch = (s->epoch + 1) & 0x07FFFFFF;
-  if (s->epoch == 0) s->epoch = 1;
+  if (s->epoch == 0) {
+    s->epoch = 1;
+    s->counters_stale = true;
+  }
   return s->epoch;
+}
+
+// Zero the launch-wide unit counter and the per-head arrival counters of a
+// session's workspace if its epoch wrapped since the last launch.
+sr_status clear_stale_counters(sr_session* s, cudaStream_t st) {
+  if (!s->counters_stale) return SR_OK;
+  if (s->buf.workspace != nullptr &&
+      sr::launch_zero_words(static_cast<int32_t*>(s->buf.workspace),
+                            static_cast<int>(sr::kWsUnitCtrBytes / 4) + s->cfg.n_heads, st) != cudaSuccess)
+    return SR_ERR_CUDA;
+  s->counters_stale = false;
+  return SR_OK;
 }
 
 // Fill one session's segment maps for `step` (rows of the chunk taken from
@@ -619,7 +620,7 @@ sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const vo
   s->lq = s->tokens_per_frame * cfg->chunk_frames;
   s->scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / std::sqrt(static_cast<float>(cfg->head_dim));
   s->n_committed = 0;
-  build_rope_tables(s);
+  sr::rope_phase_table(cfg->rope_base, cfg->head_dim, &s->phase);
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -652,7 +653,7 @@ sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs, const vo
 }
 
 sr_status sr_session_restore(sr_session* s, int64_t n_committed) {
-  if (!s || n_committed < 0 || n_committed > (int64_t(1) << 40)) return SR_ERR_INVALID_ARG;
+  if (!s || n_committed < 0 || n_committed > kMaxFrames) return SR_ERR_INVALID_ARG;
   s->n_committed = n_committed;
   return SR_OK;
 }
@@ -698,11 +699,7 @@ static sr_status rope_common(sr_session* s, int64_t first_frame, int64_t n_frame
   p.chunk_frames = static_cast<int32_t>(n_frames - first);
   p.t_clock0 = s->cfg.t_clock0;
   p.mode = mode;
-  for (int i = 0; i < 64; ++i) {
-    p.inv_freq_hi[i] = static_cast<float>(s->inv_freq[i]);
-    p.inv_freq_lo[i] = static_cast<float>(s->inv_freq[i] - static_cast<double>(p.inv_freq_hi[i]));
-  }
-  std::memcpy(p.axis, s->axis, sizeof(p.axis));
+  p.phase = s->phase;
   p.dev_n = dev_n;   // when set, first_frame is an offset from the device counter
   cudaError_t e = sr::launch_rope(p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SR_OK : SR_ERR_CUDA;
@@ -738,6 +735,7 @@ sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream) {
 sr_status sr_cache_commit_frames(sr_session* s, int32_t n_frames, const void* k_raw, const void* v, void* stream) {
   if (!s || !k_raw || !v || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
   if (!aligned16(k_raw) || !aligned16(v)) return SR_ERR_ALIGN;
+  if (s->n_committed + n_frames > kMaxFrames) return SR_ERR_STATE;
   if (s->cfg.window_frames == 0) {
     s->n_committed += n_frames;
     return SR_OK;
@@ -788,8 +786,10 @@ static sr_status attention_view(sr_session* s, const ChunkView& view, int32_t st
     p->err_word = s->buf.err_word;
     p->timeout_ns = s->cfg.wait_timeout_ns;
     set_units(*p, n_units, s);
-    cudaError_t e = sr::launch_attention_1(*p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) st = SR_ERR_CUDA;
+    st = clear_stale_counters(s, static_cast<cudaStream_t>(stream));
+    if (st == SR_OK &&
+        sr::launch_attention_1(*p, s->cfg.head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      st = SR_ERR_CUDA;
   }
   delete p;
   return st;
@@ -836,6 +836,7 @@ sr_status sr_cache_commit_dev(sr_session* s, int32_t n_frames, const void* k_raw
   if (!s || !k_raw || !v || !frames_ok(s, n_frames)) return SR_ERR_INVALID_ARG;
   if (!s->buf.frame_counter) return SR_ERR_STATE;
   if (!aligned16(k_raw) || !aligned16(v)) return SR_ERR_ALIGN;
+  if (s->n_committed + n_frames > kMaxFrames) return SR_ERR_STATE;
   sr_status st = SR_OK;
   if (s->cfg.window_frames > 0)   // frame times and slots from the device counter (offset 0)
     st = rope_common(s, 0, n_frames, k_raw, v, s->buf.ring_k, s->buf.ring_v, 1, stream, s->buf.frame_counter);
@@ -904,8 +905,10 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
       p->unit_ctr = static_cast<unsigned long long*>(s->buf.workspace);
       p->epoch = next_epoch(s);
     }
-    cudaError_t e = sr::launch_attention_n(*p, s->cfg.head_dim, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) st = SR_ERR_CUDA;
+    st = clear_stale_counters(s, static_cast<cudaStream_t>(stream));
+    if (st == SR_OK &&
+        sr::launch_attention_n(*p, s->cfg.head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      st = SR_ERR_CUDA;
   }
   delete p;
   return st;
@@ -973,8 +976,10 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
     p->err_word = s0->buf.err_word;
     p->timeout_ns = s0->cfg.wait_timeout_ns;
     set_units(*p, units, sessions[order[0]]);
-    cudaError_t e = sr::launch_attention_n(*p, s0->cfg.head_dim, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) st = SR_ERR_CUDA;
+    for (int i = 0; st == SR_OK && i < n; ++i) st = clear_stale_counters(sessions[i], static_cast<cudaStream_t>(stream));
+    if (st == SR_OK &&
+        sr::launch_attention_n(*p, s0->cfg.head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      st = SR_ERR_CUDA;
   }
   delete p;
   return st;
@@ -1050,6 +1055,19 @@ sr_status sr_plan_window(int32_t grid_h, int32_t grid_w, int32_t window, int32_t
   if (index < 0 || index >= nr * nc) return SR_ERR_INVALID_ARG;
   axis_window(grid_h, window, off, index / nc, out->row0, out->rows);
   axis_window(grid_w, window, off, index % nc, out->col0, out->cols);
+  return SR_OK;
+}
+
+sr_status sr_rope_angle(const sr_config* cfg, int32_t pair, int64_t position, float* angle) {
+  if (!cfg || !angle) return SR_ERR_INVALID_ARG;
+  sr_status st = validate_config(*cfg);
+  if (st != SR_OK) return st;
+  if (pair < 0 || pair >= cfg->head_dim / 2 || position <= -sr::kRopePositionLimit ||
+      position >= sr::kRopePositionLimit)
+    return SR_ERR_INVALID_ARG;
+  sr::RopePhase ph;
+  sr::rope_phase_table(cfg->rope_base, cfg->head_dim, &ph);
+  *angle = sr::rope_angle(ph.turn_hi[pair], ph.turn_lo[pair], position, ph.rad_hi, ph.rad_lo);
   return SR_OK;
 }
 

@@ -31,6 +31,19 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, uns
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Plain launch whose status is the launch's own: the <<<>>> form reports
+// failures only through cudaGetLastError, which would also return (and clear)
+// an unrelated error the caller left pending.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_plain(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st,
+                                Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------ attention
 // One session's view for one launch: up to four key/value segments -- the sink
 // bank of the step, the visible ring frames as one or two contiguous row
@@ -99,9 +112,45 @@ cudaError_t launch_attention_n(const AttnParams<kAttnMaxBatch>& p, int head_dim,
 int sm_count();   // SMs of the current device
 
 // ------------------------------------------------------------ RoPE / commit
+// Rotary pairs of a head: pair p (dims 2p, 2p+1) belongs to axis t, h or w and
+// turns by c_p = base^(-2i/d_axis) / (2 pi) turns per position step, held as
+// the 96-bit binary fraction C_p = round(c_p * 2^96) = turn_hi * 2^32 + turn_lo
+// (computed on the host in rope_phase.cu).
+constexpr int kMaxPairs = 64;
+struct RopePhase {
+  uint64_t turn_hi[kMaxPairs];
+  uint32_t turn_lo[kMaxPairs];
+  int8_t axis[kMaxPairs];      // 0 = t, 1 = h, 2 = w
+  float rad_hi, rad_lo;        // 2 pi / 2^32 = rad_hi + rad_lo
+};
+void rope_phase_table(float base, int head_dim, RopePhase* out);
+
+// Positions whose angle rope_angle forms exactly: |pos| < 2^42 keeps the
+// rounding of C_p below 2^-55 turns.
+constexpr int64_t kRopePositionLimit = int64_t(1) << 42;
+
+// The angle, in radians reduced into [-pi, pi), of a pair with turn constant
+// (hi, lo) at integer position pos, |pos| < kRopePositionLimit. The phase
+// frac(pos * C / 2^96), in units of 2^-64 turn, is formed with 64-bit integer
+// arithmetic (wrapping modulo 2^64 drops whole turns and nothing else), read
+// as a signed turn in [-1/2, 1/2) and scaled by 2 pi in two float parts. The
+// host and the kernels run this same function; every float operation is
+// exact or an explicit fmaf, so both get the same bits.
+__host__ __device__ inline float rope_angle(uint64_t hi, uint32_t lo, int64_t pos, float rad_hi, float rad_lo) {
+  const uint64_t a = pos < 0 ? 0ull - static_cast<uint64_t>(pos) : static_cast<uint64_t>(pos);
+  // floor(a * C / 2^32) mod 2^64 = a * hi + floor(a * lo / 2^32)
+  uint64_t ph = a * hi + (a >> 32) * lo + (((a & 0xffffffffull) * lo) >> 32);
+  if (pos < 0) ph = 0ull - ph;   // frac(-x) = -frac(x) modulo one turn
+  const int64_t s = static_cast<int64_t>(ph);
+  const int32_t w = static_cast<int32_t>(s >> 32);   // turns in units of 2^-32
+  const float f_hi = static_cast<float>(w);          // rounded; the rest goes to f_lo
+  const float f_lo = fmaf(static_cast<float>(static_cast<uint32_t>(s)), 0x1p-32f,
+                          static_cast<float>(static_cast<int64_t>(w) - static_cast<int64_t>(f_hi)));
+  return fmaf(f_hi, rad_hi, fmaf(f_hi, rad_lo, f_lo * rad_hi));
+}
+
 struct RopeParams {
-  float inv_freq_hi[64];       // per rotary pair: base^(-2i/d_axis) = hi + lo (two floats)
-  float inv_freq_lo[64];
+  RopePhase phase;
   const __nv_bfloat16* src0;   // rotated
   const __nv_bfloat16* src1;   // rotated (mode 0) or copied (mode 1)
   __nv_bfloat16* dst0;
@@ -116,7 +165,6 @@ struct RopeParams {
   int32_t chunk_frames;        // F (mode 1)
   int32_t t_clock0;
   int32_t mode;                // 0: rotate src0->dst0 and src1->dst1 in place; 1: commit
-  int8_t axis[64];             // 0 = t, 1 = h, 2 = w
   const int64_t* dev_n;        // device frame counter: when set, frame f's time and slot use
                                // *dev_n + n_committed + f (n_committed is then an offset)
 };
@@ -128,6 +176,7 @@ cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t
 cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, int32_t* ws_ctr, int n_ctr,
                                    cudaStream_t st);
 cudaError_t launch_advance_frames(int64_t* counter, int64_t add, cudaStream_t st);
+cudaError_t launch_zero_words(int32_t* words, int n, cudaStream_t st);
 
 constexpr int kMaxTailSplit = SR_MAX_TAIL_SPLIT;
 

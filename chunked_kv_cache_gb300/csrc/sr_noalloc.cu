@@ -14,12 +14,15 @@
 // loads the library holds it until the process exits. In host code its name is
 // only a host-side stand-in, never a device address: the device address is
 // obtained once per device with cudaGetSymbolAddress (with that device
-// current) and handed to the kernels as a pointer. Every call shares the
+// current; again if the device's context has been replaced, e.g. after
+// cudaDeviceReset) and handed to the kernels as a pointer. Every call shares the
 // array and finds the previous call's contents in it, so the arrival counters
 // that must start at zero are cleared on the stream before each launch, and
 // calls that overlap on the GPU (on different streams, or sessions used
 // concurrently) race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdint>
 #include <mutex>
@@ -43,18 +46,48 @@ __global__ void clear_arrival_counters(int n) {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of the scratch array on the current device, looked up once
-// per device; nullptr if the lookup fails.
+// The current context's process-unique id (cuCtxGetId), or 0 if the driver
+// cannot say. A context torn down and created again (cudaDeviceReset, then
+// more work on the device) gets a new id, and the array a new address.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context. The
+// set-up looks it up with cudaGetSymbolAddress once per device (with that
+// device current) and again only if the device's context was replaced since;
+// nullptr if the lookup fails.
 void* scratch_address() {
   static std::mutex mu;
   static void* addr[kMaxDevices];
+  static unsigned long long ctx_id[kMaxDevices];
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long id = current_context_id();   // 0: no context yet, or no id
   std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || id == 0 || id != ctx_id[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess) return nullptr;
     addr[dev] = p;
+    ctx_id[dev] = current_context_id();   // the lookup has made the context current
   }
   return addr[dev];
 }
@@ -70,8 +103,9 @@ sr_status sr_chunk_attention_noalloc(sr_session* s, int32_t step, const void* q,
   void* scratch = scratch_address();
   if (scratch == nullptr) return SR_ERR_CUDA;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  clear_arrival_counters<<<1, 256, 0, cs>>>(static_cast<int>(sr::kWsUnitCtrBytes / 4) + sr::session_heads(s));
-  if (cudaGetLastError() != cudaSuccess) return SR_ERR_CUDA;
+  if (sr::launch_plain(clear_arrival_counters, 1, 256, cs,
+                       static_cast<int>(sr::kWsUnitCtrBytes / 4) + sr::session_heads(s)) != cudaSuccess)
+    return SR_ERR_CUDA;
   return sr::attention_into_scratch(s, step, q, k, v, o, lse, stream, scratch);
 }
 

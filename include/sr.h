@@ -147,6 +147,8 @@ SR_API sr_status sr_session_init(const sr_config* cfg, const sr_buffers* bufs,
  * n_committed frames (checkpoint / resume, or a synthetic mid-stream start):
  * frame g in slot g mod W for the last min(n_committed, W) frames, and
  * slot_frame filled accordingly. Only the host mirror of n changes.
+ * 0 <= n_committed <= 2^31 - 1 (slot_frame holds frame indices as int32), else
+ * SR_ERR_INVALID_ARG.
  */
 SR_API sr_status sr_session_restore(sr_session* s, int64_t n_committed);
 
@@ -160,8 +162,10 @@ SR_API sr_status sr_session_frames(const sr_session* s, int64_t* n_committed);
  * q, k: [F*T][H][d] bf16, rotated in place. Token n lies in frame f = n / T,
  * row (n % T) / grid_w, column n % grid_w; its time is t_clock0 + n_committed + f.
  * The head dim splits into [d_t | d_h | d_w], d_h = d_w = 2*floor(d/6); inside an
- * axis, pair (x[2i], x[2i+1]) turns by p * rope_base^(-2i/d_axis). Computed in
- * fp32, stored bf16 round-to-nearest-even. Either pointer may be NULL to skip it.
+ * axis, pair (x[2i], x[2i+1]) turns by p * rope_base^(-2i/d_axis). The angle is
+ * reduced modulo 2*pi exactly, whatever the stream time (see sr_rope_angle); the
+ * rotation is computed in fp32 and stored bf16 round-to-nearest-even. Either
+ * pointer may be NULL to skip it.
  */
 SR_API sr_status sr_rope3d_qk(sr_session* s, void* q, void* k, void* stream);
 
@@ -191,7 +195,9 @@ SR_API sr_status sr_chunk_attention(sr_session* s, int32_t step, const void* q, 
  * lives). k_raw (un-rotated) and v:
  * [F*T][H][d] bf16. Frame g = n + f goes to slot g mod W with its keys rotated at
  * time t_clock0 + g; slot_frame[g mod W] = g; then n += F. The frames previously
- * held by those slots are evicted. With W = 0 only n advances.
+ * held by those slots are evicted. With W = 0 only n advances. A session commits
+ * at most 2^31 - 1 frames (slot_frame is int32): a commit past that returns
+ * SR_ERR_STATE and changes nothing.
  */
 SR_API sr_status sr_cache_commit(sr_session* s, const void* k_raw, const void* v, void* stream);
 
@@ -305,7 +311,7 @@ SR_API sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving
 /*
  * sr_rope3d_qk for rows of n_frames frames starting at the stream's frame
  * first_frame (time t_clock0 + first_frame + f): recomputed history rows keep their
- * own frame times. |first_frame| <= 2^40.
+ * own frame times. |first_frame| <= 2^40, else SR_ERR_INVALID_ARG.
  */
 SR_API sr_status sr_rope3d_qk_at(sr_session* s, int64_t first_frame, int32_t n_frames, void* q, void* k,
                                  void* stream);
@@ -357,6 +363,23 @@ typedef struct {
 SR_API sr_status sr_window_count(int32_t grid_h, int32_t grid_w, int32_t window, int32_t shifted, int32_t* count);
 SR_API sr_status sr_plan_window(int32_t grid_h, int32_t grid_w, int32_t window, int32_t shifted, int32_t index,
                                 sr_window* out);
+
+/*
+ * The rotation angle the RoPE and commit kernels apply, as host arithmetic (no
+ * GPU call): rotary pair `pair` (0 <= pair < head_dim/2, numbered across
+ * [d_t | d_h | d_w]) of a token at integer position `position` on that pair's
+ * axis turns by theta = position * rope_base^(-2i/d_axis) ([H3 page] 3.2
+ * Iteration 4: the time position is the absolute latent-frame index of the
+ * stream, which grows without bound). *angle receives theta reduced into
+ * [-pi, pi), rounded to float. The reduction is exact: each pair's
+ * rope_base^(-2i/d_axis) / (2*pi) is held as a 96-bit binary fraction, and the
+ * phase position * that fraction modulo 1 is formed in integer arithmetic, so
+ * the angle is within about 2^-24 rad of the exact reduced value for every
+ * |position| < 2^42 (every position the other calls can produce). The kernels run
+ * the same arithmetic and then take the fp32 sine and cosine of *angle.
+ * SR_ERR_INVALID_ARG for a bad config, pair or position.
+ */
+SR_API sr_status sr_rope_angle(const sr_config* cfg, int32_t pair, int64_t position, float* angle);
 
 /* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
 SR_API sr_status sr_device_error_status(int32_t err_word_value);

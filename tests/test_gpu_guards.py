@@ -4,9 +4,10 @@ compute-sanitizer is not available on the GPU pool, so out-of-bounds writes are
 caught the old way: every buffer the library writes (sink banks, ring K/V,
 slot table, error word, workspace, the in-place Q/K and the outputs) sits
 between two guard bands filled with a canary byte, and after a run that wraps
-the ring, splits last blocks over work units and takes both denoising steps,
-every guard byte must still hold the canary. The session is built through the
-C ABI directly so that its buffers can be placed inside the guarded blocks."""
+the ring, splits last blocks over work units and takes both denoising steps
+(and one allocation-free attention call), every guard byte must still hold
+the canary. The session is built through the C ABI directly so that its
+buffers can be placed inside the guarded blocks."""
 import numpy as np
 import pytest
 import torch
@@ -87,6 +88,17 @@ def test_nothing_written_outside_the_buffers():
             N.sr_chunk_attention(handle, st, q.inner.data_ptr(), k.inner.data_ptr(), v.data_ptr(),
                                  o.inner.data_ptr(), lse.inner.data_ptr(), stream)
             outs.append((o, lse))
+        # the allocation-free entry point writes O and LSE through its own host
+        # path (its scratch is the library's built-in array): guard those too
+        q, k = Guarded(shape.lq * H * d * 2, dev), Guarded(shape.lq * H * d * 2, dev)
+        q.view(bf16, rows).copy_(to_dev(x.q[0], dev))
+        k.view(bf16, rows).copy_(to_dev(x.k[0], dev))
+        v = to_dev(x.v[0], dev)
+        o, lse = Guarded(shape.lq * H * d * 2, dev), Guarded(H * shape.lq * 4, dev)
+        guarded += [q, k, o, lse]
+        N.sr_chunk_attention_noalloc(handle, 0, q.inner.data_ptr(), k.inner.data_ptr(), v.data_ptr(),
+                                     o.inner.data_ptr(), lse.inner.data_ptr(), stream)
+        outs.append((o, lse))
         torch.cuda.synchronize()
         assert int(err.view(torch.int32, (1,)).item()) == 0
         for o, lse in outs:

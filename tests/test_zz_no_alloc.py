@@ -6,18 +6,20 @@ stream and its tensors: they cannot provide the session workspace that the key
 split of a chunk's last query block uses, so this entry point takes its scratch
 from an array built into the library instead.
 
-Checked here, through the C ABI: two calls in a row agree with
-sr_chunk_attention on the same inputs within the attention tolerances of the
-parity tests, with the key split forced on (so the built-in scratch is really
-used, and reused by the second call), and a session too large for the scratch
-is refused before anything runs. This file is collected last on purpose.
+Checked here, through the C ABI, on two calls in a row with the key split
+forced on (so the built-in scratch is really used, and reused by the second
+call): the output against the float64 oracle within the attention tolerances
+of the parity tests, and bit for bit against sr_chunk_attention on a twin
+session that has its own workspace and the same forced split (the same plan,
+so the same arithmetic). A session too large for the scratch is refused before
+anything runs. This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
 import synthetic as syn
-from tests.gpu_common import LSE_ABS, assert_attention_close, device, to_dev
+from tests.gpu_common import LSE_ABS, Twin, assert_attention_close, device, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -29,42 +31,49 @@ def _built():
     device()
 
 
-def test_noalloc_matches_sr_chunk_attention_twice():
-    import chunked_kv_cache_gb300 as sr
+def _edge_rows(lq):
+    # both query tiles of the first and last blocks, the rows around the
+    # single-tile last block (3120 = 12 * 256 + 48 rows), and a random sample
+    base = [0, 1, 127, 128, 255, 256, 1537, lq - 49, lq - 48, lq - 47, lq - 2, lq - 1]
+    rng = np.random.default_rng(11)
+    return sorted(set(base + [int(r) for r in rng.choice(lq, 40, replace=False)]))
+
+
+def test_noalloc_matches_oracle_and_sr_chunk_attention_twice():
     from chunked_kv_cache_gb300 import _native as N
-    dev = device()
     shape = syn.SHAPE_832x480
-    sk, sv = syn.session_sinks(shape, 2)
-    # no workspace of its own; the key split of the last blocks is forced to 4 parts
-    s = sr.Session(shape.n_heads, shape.head_dim, shape.grid_h, shape.grid_w, shape.chunk_frames,
-                   shape.window_frames, shape.n_sink, shape.n_steps, sink_k=to_dev(sk, dev), sink_v=to_dev(sv, dev),
-                   tail_split=4, workspace=False, device=dev)
-    rk, rv, slots = syn.ring_prefill(shape, 2, shape.window_frames)
-    s.ring_k.copy_(to_dev(rk, dev))
-    s.ring_v.copy_(to_dev(rv, dev))
-    s.slot_frame.copy_(torch.from_numpy(slots).to(dev))
-    s.restore(shape.window_frames)
+    heads = [0, 13]
+    fill = shape.window_frames
+    # the allocation-free session: no workspace of its own, last blocks forced into 4 key parts
+    tw = Twin(shape, 2, fill=fill, heads=heads, tail_split=4, workspace=False)
+    # its twin with a workspace and the same split, for the bit-for-bit check
+    twin = Twin(shape, 2, fill=fill, heads=heads, tail_split=4, workspace=True)
+    dev = tw.dev
     x = syn.chunk_inputs(shape, 2, chunk=5)
     q, k, v = (to_dev(b, dev) for b in (x.q[0], x.k[0], x.v[0]))
+    tw.gpu.rope3d_qk(q, k)                     # both sessions are at the same frame count
+    qo, ko = tw.ora.rope3d_qk(tw.oh(x.q[0]), tw.oh(x.k[0]))
+    rows = _edge_rows(shape.lq)
+    ref, ref_lse = tw.ora.chunk_attention(0, qo, ko, tw.oh(x.v[0]), rows=rows)
     stream = torch.cuda.current_stream(dev).cuda_stream
 
-    ref_o = torch.empty_like(q)
-    ref_l = torch.empty((shape.n_heads, shape.lq), dtype=torch.float32, device=dev)
-    N.sr_chunk_attention(s.handle, 0, q.data_ptr(), k.data_ptr(), v.data_ptr(), ref_o.data_ptr(),
-                         ref_l.data_ptr(), stream)
-    ref = ref_o.float().cpu().numpy().astype(np.float64)
-    ref_lse = ref_l.cpu().numpy().astype(np.float64)
+    same_o = torch.empty_like(q)
+    same_l = torch.empty((shape.n_heads, shape.lq), dtype=torch.float32, device=dev)
+    N.sr_chunk_attention(twin.gpu.handle, 0, q.data_ptr(), k.data_ptr(), v.data_ptr(), same_o.data_ptr(),
+                         same_l.data_ptr(), stream)
     for call in range(2):
         o = torch.full_like(q, float("nan"))
         lse = torch.full((shape.n_heads, shape.lq), float("nan"), dtype=torch.float32, device=dev)
-        N.sr_chunk_attention_noalloc(s.handle, 0, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+        N.sr_chunk_attention_noalloc(tw.gpu.handle, 0, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                      lse.data_ptr(), stream)
         torch.cuda.synchronize()
-        got = o.float().cpu().numpy().astype(np.float64)
-        assert_attention_close(got, ref, f"noalloc call {call}")
-        assert np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max() <= LSE_ABS
-    assert s.error_status() == 0
-    s.close()
+        got = o.float().cpu().numpy().astype(np.float64)[:, heads][rows]
+        assert_attention_close(got, ref, f"noalloc call {call} against the oracle")
+        got_lse = lse.cpu().numpy().astype(np.float64)[heads][:, rows]
+        assert np.abs(got_lse - ref_lse).max() <= LSE_ABS
+        assert torch.equal(o, same_o), f"noalloc call {call} differs from sr_chunk_attention with a workspace"
+        assert torch.equal(lse, same_l)
+    assert tw.gpu.error_status() == 0 and twin.gpu.error_status() == 0
 
 
 def test_noalloc_refuses_sessions_beyond_its_scratch():
