@@ -67,6 +67,19 @@ def _peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def _sustained_bf16():
+    """The bf16 GEMM rate held for seconds under the power cap: the peak of a
+    kernel timed inside a long, back-to-back step."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured"
+    return 1700.0, "fallback"
+
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -182,6 +195,9 @@ def run_ours(args):
     flops_chunk = shape.n_steps * flops_attn
     commit_bytes = 4 * shape.lq * shape.n_heads * shape.head_dim * 2
     sessions = [_make_session(shape, args.config, i + 10 * rank, dev) for i in range(2)]
+    session_mb = sum(t.numel() * t.element_size() for t in
+                     [sessions[0][0].sink_k, sessions[0][0].sink_v, sessions[0][0].ring_k, sessions[0][0].ring_v] +
+                     [v for val in sessions[0][1].values() for v in (val if isinstance(val, list) else [val])]) / 1e6
     # A bench step is R chunks, enough for tens of milliseconds, so that the
     # clock sampler sees the GPU under load many times over the timed steps.
     R = args.chunks_per_step or CHUNKS_PER_STEP[args.config]
@@ -234,6 +250,7 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     peak_tf, peak_gbs, peak_kind = _peaks()
+    sus_tf, sus_kind = _sustained_bf16()
     attn_avg = statistics.mean(attn_ms)
     achieved = flops_attn / (attn_avg / 1e3) / 1e12
     value = aggregate_throughput(n_chunks * flops_chunk, elapsed, world) / 1e12
@@ -253,14 +270,17 @@ def run_ours(args):
                                "2 x (RoPE-3D + chunk attention) + ring commit",
                    "heads": shape.n_heads, "head_dim": shape.head_dim, "lq": shape.lq,
                    "lk": shape.lk(full), "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: two ~280 MB sessions used alternately"},
+                   "l2": f"inputs larger than L2: two sessions of {session_mb:.0f} MB used alternately"},
         "attention_ms_per_denoise_step": round(attn_avg, 4),
         "attention_ms_p10_p50_p90": [round(float(np.percentile(attn_ms, q)), 4) for q in (10, 50, 90)],
         "attention_tflops": round(achieved, 2),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_tf, 4), "traffic": traffic,
+        # the attention launches run back to back for about a second under the
+        # power cap: the sustained bf16 rate is their peak (burst beside it)
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": sus_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / sus_tf, 4), "traffic": traffic,
                      "kernel": "attn_kernel (sr_chunk_attention)",
-                     "peak_kind": f"{peak_kind} bf16 dense burst",
+                     "peak_kind": f"{sus_kind} bf16 dense sustained (seconds-long GEMM loop under the power cap)",
+                     "burst_peak": peak_tf, "frac_of_burst": round(achieved / peak_tf, 4),
                      "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4),
                      "nominal_peak": f"{NOMINAL_BF16_TFLOPS:.0f} TFLOP/s nominal dense bf16 (spec, not measured)"},
         "kernels": {
