@@ -820,7 +820,10 @@ def run_decoder(args):
     its chunk (1541 keys for a full window). Latent grids of the 720p and the
     pages' 768x1344 streams; 16 heads x 128 (a synthetic model shape: the pages
     give no head count). Plain and shifted layers (the shifted one has partial
-    windows at the edges); attention only, inputs already packed per window."""
+    windows at the edges). A layer per chunk = the window gather of frame-major
+    Q, K, V with RoPE (one launch), the batched attention (one launch) and the
+    commit of the clean K, V into every window's ring (one launch); each part is
+    also timed alone."""
     world, rank, local = _dist()
     if rank != 0:
         return
@@ -829,72 +832,103 @@ def run_decoder(args):
     from chunked_kv_cache_gb300 import build
     build.build()
     from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
-    H, d, G = 16, 128, 5
+    H, d, G, F = 16, 128, 5, 2
     grids = {"720p (45x80 tokens)": (45, 80), "768x1344 (48x84 tokens)": (48, 84)}
     results, lay_fl = {}, {}
-    peak_tf, _, peak_kind = _peaks()
+    peak_tf, peak_gbs, peak_kind = _peaks()
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    def replay_ms(fn):
+        """Device time of one CUDA-graph replay of fn's launches (no host work per call)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        return timed(g.replay)
+
     for gname, (gh, gw) in grids.items():
         for shifted in (False, True):
-            lay = DecoderWindowLayer(gh, gw, H, d, G, shifted=shifted, device=dev)
-            rows = lay.rows
-            mk = lambda tid: syn.device_normal_bf16((rows, H, d), dev, 8, int(shifted), 0, 0, tid)
+            lay = DecoderWindowLayer(gh, gw, H, d, G, shifted=shifted, chunk_frames=F, device=dev)
+            dims = (F, gh, gw, H, d)
+            mk = lambda tid: syn.device_normal_bf16(dims, dev, 8, int(shifted), 0, 0, tid)
             q, k, v = mk(syn.T_Q), mk(syn.T_K), mk(syn.T_V)
             ck, cv = mk(syn.T_CLEAN_K), mk(syn.T_CLEAN_V)
             lay.set_global(syn.device_normal_bf16((G, H, d), dev, 8, 0, 0, 0, syn.T_SINK_K),
                            syn.device_normal_bf16((G, H, d), dev, 8, 0, 0, 0, syn.T_SINK_V))
             for _ in range(2):                     # fill the 4-frame caches
                 lay.commit(ck, cv)
-            o = torch.empty_like(q)
+            packed = tuple(torch.empty((lay.rows, H, d), dtype=torch.bfloat16, device=dev) for _ in range(3))
+            o = torch.empty_like(packed[0])
+
+            def layer():
+                qp, kp, vp = lay.gather_rope(q, k, v, out=packed)
+                lay.attention(qp, kp, vp, out=o)
+                lay.commit(ck, cv)
+
             for _ in range(max(args.warmup, 3)):
-                lay.attention(q, k, v, out=o)
+                layer()
             torch.cuda.synchronize()
-            def timed(fn):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                for _ in range(args.steps):
-                    fn()
-                b.record()
-                torch.cuda.synchronize()
-                return a.elapsed_time(b) / args.steps
-            eager_ms = timed(lambda: lay.attention(q, k, v, out=o))
-            # the same layer replayed from a CUDA graph: the device time without
-            # the host's per-call work (up to 24 windows' tensor maps per launch)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                lay.attention(q, k, v, out=o)
-            for _ in range(3):
-                g.replay()
-            torch.cuda.synchronize()
-            ms = timed(g.replay)
+            eager_ms = timed(layer)
+            layer_ms = replay_ms(layer)
+            gather_ms = replay_ms(lambda: lay.gather_rope(q, k, v, out=packed))
+            attn_ms = replay_ms(lambda: lay.attention(*packed, out=o))
+            commit_ms = replay_ms(lambda: lay.commit(ck, cv))
             fl = sum(4.0 * H * s.lq * (G + 6 * s.T) * d for s in lay.sessions)
+            tok_bytes = F * gh * gw * H * d * 2                 # one tensor of the chunk
+            gather_bytes, commit_bytes = 6 * tok_bytes, 4 * tok_bytes
             full = [s for s in lay.sessions if s.T == 256]
-            lay_fl[f"{gname}, {'shifted' if shifted else 'plain'} layer"] = fl
-            results[f"{gname}, {'shifted' if shifted else 'plain'} layer"] = {
-                "windows": len(lay.windows), "full_windows": len(full), "launches": len(lay.groups),
-                "ms_per_layer": round(ms, 4), "tflops": round(fl / (ms / 1e3) / 1e12, 2),
-                "eager_ms_per_layer": round(eager_ms, 4)}
+            name = f"{gname}, {'shifted' if shifted else 'plain'} layer"
+            lay_fl[name] = fl
+            results[name] = {
+                "windows": len(lay.windows), "full_windows": len(full),
+                "launches": len(lay.groups) + 2 * len(lay.layer_groups),
+                "ms_per_layer": round(layer_ms, 4), "eager_ms_per_layer": round(eager_ms, 4),
+                "attention_ms": round(attn_ms, 4), "attention_tflops": round(fl / (attn_ms / 1e3) / 1e12, 2),
+                "gather_rope_us": round(gather_ms * 1e3, 2),
+                "gather_rope_GBs": round(gather_bytes / (gather_ms / 1e3) / 1e9, 1),
+                "gather_rope_frac_hbm": round(gather_bytes / (gather_ms / 1e3) / 1e9 / peak_gbs, 4),
+                "commit_us": round(commit_ms * 1e3, 2),
+                "commit_GBs": round(commit_bytes / (commit_ms / 1e3) / 1e9, 1),
+                "commit_frac_hbm": round(commit_bytes / (commit_ms / 1e3) / 1e9 / peak_gbs, 4),
+                "share_of_layer": {"gather_rope": round(gather_ms / layer_ms, 3),
+                                   "attention": round(attn_ms / layer_ms, 3),
+                                   "commit": round(commit_ms / layer_ms, 3)}}
             if lay.error_status() != 0:
                 raise RuntimeError("device error word set during the bench")
             lay.close()
     key = "768x1344 (48x84 tokens), shifted layer"
     rate, done, used = _oracle_attention_rate([(512, G + 6 * 256)], d)
     out = {
-        "metric": "decoder window attention ms per layer on 1 GB300", "value": results[key]["ms_per_layer"],
+        "metric": "decoder window-attention layer ms on 1 GB300 (window gather + RoPE, attention, cache commit)",
+        "value": results[key]["ms_per_layer"],
         "unit": "ms/layer", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "streaming decoder layer: 16x16-token windows, 2-frame chunk, 4 cached frames, "
-                               "5 global tokens, 16 heads x 128 (synthetic); windows batched per launch "
-                               "(at most 24); full cache; attention only; ms_per_layer from a CUDA-graph "
-                               "replay of the layer's launches (eager_ms_per_layer: issued call by call)"},
+                               "5 global tokens, 16 heads x 128 (synthetic); frame-major Q, K, V gathered per "
+                               "window with RoPE in one launch, every window's attention in one launch (at most "
+                               "24 windows), every window's cache commit in one launch; full cache; ms_per_layer "
+                               "from a CUDA-graph replay of the layer's launches (eager_ms_per_layer: issued call "
+                               "by call); each part also replayed alone"},
         "layers": results,
         "context": "pages: FlexAttention with a block mask, 6 ms per layer on GB200 (their 1.62B decoder)",
-        "roofline": {"bound": "tensor", "achieved": results[key]["tflops"], "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": round(results[key]["tflops"] / peak_tf, 4),
-                     "kernel": "attn_kernel<128,24> (sr_chunk_attention_batch)", "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "roofline": {"bound": "tensor", "achieved": results[key]["attention_tflops"], "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(results[key]["attention_tflops"] / peak_tf, 4),
+                     "kernel": "attn_kernel<128,24> (sr_chunk_attention_batch)",
+                     "peak_kind": f"{peak_kind} bf16 dense burst"},
         "cpu_baseline": _oracle_line(rate, done, used, "one full window (512 queries x 1541 keys); ms per layer "
-                                     "extrapolated to every window and head of the " + key,
+                                     "extrapolated to every window and head of the " + key + " (attention only)",
                                      value=round(lay_fl[key] / rate * 1e3, 2), unit="ms/layer"),
-        "gpu_launches": 2 * sum(v["launches"] for v in results.values()) * args.steps,
+        "gpu_launches": sum(v["launches"] for v in results.values()) * args.steps * 3,
     }
     print(json.dumps(out), flush=True)
 

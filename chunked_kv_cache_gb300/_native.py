@@ -21,6 +21,7 @@ SR_ERR_CUDA = -5
 SR_ERR_TIMEOUT = -6
 SR_DEVERR_WAIT_TIMEOUT = 1
 SR_MAX_BATCH = 24
+SR_MAX_LAYER_WINDOWS = 96
 
 # every extern "C" symbol that include/sr.h declares
 EXPORTS = (
@@ -30,7 +31,7 @@ EXPORTS = (
     "sr_chunk_attention_noalloc", "sr_plan_chunk", "sr_rope3d_qk_frames", "sr_chunk_attention_frames",
     "sr_cache_commit_frames", "sr_window_attention", "sr_rope3d_qk_at", "sr_rope3d_qk_dev",
     "sr_chunk_attention_dev", "sr_cache_commit_dev", "sr_window_count", "sr_plan_window",
-    "sr_plan_attention", "sr_rope_angle",
+    "sr_plan_attention", "sr_rope_angle", "sr_layer_rope_gather", "sr_layer_commit",
 )
 
 
@@ -110,6 +111,9 @@ def lib() -> ctypes.CDLL:
         L.sr_plan_attention.argtypes = [i32, i64, i64, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                         ctypes.POINTER(i64)]
         L.sr_rope_angle.argtypes = [ctypes.POINTER(SrConfig), i32, i64, ctypes.POINTER(ctypes.c_float)]
+        L.sr_layer_rope_gather.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(SrWindow), i32, i32, i32, vp, vp, vp,
+                                           vp, vp, vp, vp]
+        L.sr_layer_commit.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(SrWindow), i32, i32, i32, vp, vp, vp]
         L.sr_device_error_status.argtypes = [i32]
         L.sr_debug_wait_timeout.argtypes = [vp, u64, vp]
         L.sr_workspace_bytes.argtypes = [ctypes.POINTER(SrConfig), ctypes.POINTER(ctypes.c_uint64)]
@@ -266,6 +270,28 @@ def sr_rope_angle(cfg: SrConfig, pair: int, position: int) -> float:
     a = ctypes.c_float()
     _check(lib().sr_rope_angle(ctypes.byref(cfg), int(pair), int(position), ctypes.byref(a)), "sr_rope_angle")
     return a.value
+
+
+def _layer_args(handles, windows):
+    n = len(handles)
+    arr = (ctypes.c_void_p * n)(*handles)
+    wins = (SrWindow * n)(*[SrWindow(w.row0, w.col0, w.rows, w.cols) for w in windows])
+    return arr, wins, n
+
+
+def sr_layer_rope_gather(handles, windows, frame_h: int, frame_w: int, q: int, k: int, v: int, q_packed: int,
+                         k_packed: int, v_packed: int, stream: int) -> None:
+    """A decoder layer's window gather with RoPE (q, k) and copy (v, optional), one launch."""
+    arr, wins, n = _layer_args(handles, windows)
+    _check(lib().sr_layer_rope_gather(arr, wins, n, int(frame_h), int(frame_w), q, k, v or None, q_packed, k_packed,
+                                      v_packed or None, stream or None), "sr_layer_rope_gather")
+
+
+def sr_layer_commit(handles, windows, frame_h: int, frame_w: int, k_raw: int, v: int, stream: int) -> None:
+    """Every window's ring commit of a decoder layer, one launch."""
+    arr, wins, n = _layer_args(handles, windows)
+    _check(lib().sr_layer_commit(arr, wins, n, int(frame_h), int(frame_w), k_raw, v, stream or None),
+           "sr_layer_commit")
 
 
 def sr_device_error_status(value: int) -> int:

@@ -175,6 +175,176 @@ cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st) {
   }
 }
 
+// ------------------------------------------------------------ decoder layers
+// All windows of a decoder layer in one launch. A CTA takes whole tokens of
+// one window (the host gives each window a contiguous range of CTAs). Mode 0
+// gathers the window's tokens from the frame-major q, k, v into the packed
+// layout the batched attention reads, rotating q and k at window-relative
+// (h, w) and absolute frame time; mode 1 writes the window's frames of the
+// clean k (rotated) and v into the window's ring slots and its slot table.
+// Per token the source row is (f * frame_h + row0 + r) * frame_w + col0 + c;
+// every row is H*d contiguous elements, so loads and stores stay coalesced.
+
+namespace {
+
+template <int D>
+__global__ void __launch_bounds__(kRopeThreads) layer_rope_kernel(const LayerRopeParams p) {
+  constexpr int kPairs = D / 2;
+  constexpr int kVecPerHead = D / 8;
+  grid_dep_wait();   // the previous kernel of the stream may still be draining
+  grid_dep_launch_dependents();
+  extern __shared__ float2 smem_layer[];
+  const int tpc = p.tokens_per_cta;
+  float2* cs_table = smem_layer;                                             // [tpc][D/2]
+  int64_t* src_row = reinterpret_cast<int64_t*>(cs_table + tpc * kPairs);   // [tpc]
+  int64_t* dst_row = src_row + tpc;                                          // [tpc]
+  int32_t* pos = reinterpret_cast<int32_t*>(dst_row + tpc);                  // [tpc][3]: frame, row, column
+
+  // this CTA's window: the last one whose first CTA is not after this CTA
+  int wi = 0;
+  for (int i = 1; i < p.n_windows; ++i)
+    if (p.win[i].cta_begin <= static_cast<int>(blockIdx.x)) wi = i;
+  const int row0 = p.win[wi].row0, col0 = p.win[wi].col0, cols = p.win[wi].cols;
+  const int T_w = p.win[wi].rows * cols;
+  const int64_t n0 = p.win[wi].n_committed;
+  const int first = p.win[wi].first_frame;
+  const int wf = p.win[wi].window_frames;
+  const int tok_lo = (static_cast<int>(blockIdx.x) - p.win[wi].cta_begin) * tpc;
+  const int ntok = min(tpc, p.win[wi].n_tok - tok_lo);
+  if (ntok <= 0) return;
+  const int vpt = p.n_heads * kVecPerHead;   // 16-byte vectors per token
+  const int nvec = ntok * vpt;
+  const bool commit = p.mode == 1;
+
+  // the window's slot table: frame g = n + f now lives in slot g mod W
+  if (commit && tok_lo == 0) {
+    int32_t* slots = p.win[wi].slot_frame;
+    const int frames = p.win[wi].n_tok / T_w;
+    for (int f = threadIdx.x; f < frames; f += kRopeThreads) {
+      const int64_t g = n0 + first + f;
+      slots[g % wf] = static_cast<int32_t>(g);
+    }
+  }
+
+  // source row, destination row and (frame, row, column) of every token
+  for (int t = threadIdx.x; t < ntok; t += kRopeThreads) {
+    const int j = first * T_w + tok_lo + t;   // token of the window's chunk, frame by frame
+    const int f = j / T_w;
+    const int rc = j - f * T_w;
+    const int r = rc / cols;
+    const int c = rc - r * cols;
+    src_row[t] = (static_cast<int64_t>(f) * p.frame_h + row0 + r) * p.frame_w + col0 + c;
+    dst_row[t] = commit ? static_cast<int64_t>((n0 + f) % wf) * T_w + rc : p.win[wi].packed_row0 + j;
+    pos[3 * t] = f;
+    pos[3 * t + 1] = r;
+    pos[3 * t + 2] = c;
+  }
+  __syncthreads();
+
+  const uint4* s0 = reinterpret_cast<const uint4*>(p.src[0]);
+  const uint4* s1 = reinterpret_cast<const uint4*>(p.src[1]);
+  const uint4* s2 = reinterpret_cast<const uint4*>(p.src[2]);   // NULL: no third tensor
+  uint4* d0 = reinterpret_cast<uint4*>(commit ? p.win[wi].ring_k : p.dst[0]);
+  uint4* d1 = reinterpret_cast<uint4*>(commit ? p.win[wi].ring_v : p.dst[1]);
+  uint4* d2 = reinterpret_cast<uint4*>(p.dst[2]);
+
+  for (int base = 0; base < nvec; base += kRopeVecTarget) {
+    // loads first: they are in flight while the sin/cos table is built
+    uint4 a[kRopeVecPerThread], b[kRopeVecPerThread], c3[kRopeVecPerThread];
+    {
+      int j = base + threadIdx.x;
+      int t = j / vpt;
+      int r = j - t * vpt;
+#pragma unroll
+      for (int k = 0; k < kRopeVecPerThread; ++k) {
+        if (j < nvec) {
+          const int64_t at = src_row[t] * vpt + r;
+          a[k] = s0[at];
+          b[k] = s1[at];
+          if (s2 != nullptr) c3[k] = s2[at];
+        }
+        j += kRopeThreads;
+        r += kRopeThreads;
+        while (r >= vpt) {
+          r -= vpt;
+          ++t;
+        }
+      }
+    }
+
+    if (base == 0) {
+      for (int i = threadIdx.x; i < ntok * kPairs; i += kRopeThreads) {
+        const int t = i / kPairs;
+        const int pr = i - t * kPairs;
+        const int ax = p.phase.axis[pr];
+        const int64_t ps = ax == 0 ? p.t_clock0 + n0 + pos[3 * t] : pos[3 * t + ax];
+        const float ang = rope_angle(p.phase.turn_hi[pr], p.phase.turn_lo[pr], ps, p.phase.rad_hi, p.phase.rad_lo);
+        float sn, cs;
+        sincosf(ang, &sn, &cs);
+        cs_table[i] = make_float2(cs, sn);
+      }
+      __syncthreads();
+    }
+
+    int j = base + threadIdx.x;
+    int t = j / vpt;
+    int r = j - t * vpt;
+#pragma unroll
+    for (int k = 0; k < kRopeVecPerThread; ++k) {
+      if (j < nvec) {
+        const float2* cs = cs_table + t * kPairs + (r & (kVecPerHead - 1)) * 4;
+        uint32_t* wa = reinterpret_cast<uint32_t*>(&a[k]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wa[q] = rotate_pair(wa[q], cs[q].x, cs[q].y);
+        if (!commit) {   // gather: q and k rotate, v is copied; commit: k rotates, v is copied
+          uint32_t* wb = reinterpret_cast<uint32_t*>(&b[k]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) wb[q] = rotate_pair(wb[q], cs[q].x, cs[q].y);
+        }
+        const int64_t at = dst_row[t] * vpt + r;
+        d0[at] = a[k];
+        d1[at] = b[k];
+        if (s2 != nullptr) d2[at] = c3[k];
+      }
+      j += kRopeThreads;
+      r += kRopeThreads;
+      while (r >= vpt) {
+        r -= vpt;
+        ++t;
+      }
+    }
+  }
+}
+
+size_t layer_smem_bytes(int tpc, int head_dim) {
+  return static_cast<size_t>(tpc) * ((head_dim / 2) * sizeof(float2) + 2 * sizeof(int64_t) + 3 * sizeof(int32_t));
+}
+
+}  // namespace
+
+int layer_tokens_per_cta(int n_heads, int head_dim) {
+  return std::max(1, kRopeVecTarget / (n_heads * head_dim / 8));
+}
+
+cudaError_t launch_layer_rope(const LayerRopeParams& p, int head_dim, int n_ctas, cudaStream_t st) {
+  if (n_ctas <= 0) return cudaSuccess;
+  const size_t smem = layer_smem_bytes(p.tokens_per_cta, head_dim);
+  if (head_dim == 128) {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(layer_rope_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    return launch_dependent(layer_rope_kernel<128>, static_cast<unsigned>(n_ctas), kRopeThreads, smem, st, p);
+  }
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(layer_rope_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_dependent(layer_rope_kernel<64>, static_cast<unsigned>(n_ctas), kRopeThreads, smem, st, p);
+}
+
 // ------------------------------------------------------------ small helpers
 
 namespace {

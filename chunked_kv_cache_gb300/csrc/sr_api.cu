@@ -985,6 +985,105 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
   return st;
 }
 
+// A decoder layer's windows in one launch (sr_layer_rope_gather, mode 0, and
+// sr_layer_commit, mode 1): validate that the sessions form one layer of the
+// frame, then give each window a contiguous range of CTAs.
+static sr_status layer_common(sr_session* const* ss, const sr_window* wins, int32_t n, int32_t fh, int32_t fw,
+                              const void* s0, const void* s1, const void* s2, void* d0, void* d1, void* d2,
+                              int mode, void* stream) {
+  if (!ss || !wins || n < 1 || n > SR_MAX_LAYER_WINDOWS || fh < 1 || fw < 1 || !s0 || !s1) return SR_ERR_INVALID_ARG;
+  if (mode == 0 && (!d0 || !d1 || ((s2 == nullptr) != (d2 == nullptr)))) return SR_ERR_INVALID_ARG;
+  const void* ptrs[6] = {s0, s1, s2, d0, d1, d2};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return SR_ERR_ALIGN;
+  const sr_session* a = ss[0];
+  if (!a) return SR_ERR_INVALID_ARG;
+  const int64_t F = a->cfg.chunk_frames;
+  const int64_t row_elems = static_cast<int64_t>(a->cfg.n_heads) * a->cfg.head_dim;
+  const int64_t frame_rows = static_cast<int64_t>(fh) * fw * F;
+  if (frame_rows > (int64_t(1) << 28) || frame_rows * row_elems > (int64_t(1) << 40)) return SR_ERR_INVALID_ARG;
+  int64_t packed = 0;
+  for (int i = 0; i < n; ++i) {
+    const sr_session* s = ss[i];
+    const sr_window& w = wins[i];
+    if (!s || s->cfg.n_heads != a->cfg.n_heads || s->cfg.head_dim != a->cfg.head_dim ||
+        s->cfg.chunk_frames != F || s->cfg.t_clock0 != a->cfg.t_clock0 || s->cfg.rope_base != a->cfg.rope_base)
+      return SR_ERR_INVALID_ARG;
+    if (w.rows != s->cfg.grid_h || w.cols != s->cfg.grid_w || w.row0 < 0 || w.col0 < 0 ||
+        static_cast<int64_t>(w.row0) + w.rows > fh || static_cast<int64_t>(w.col0) + w.cols > fw)
+      return SR_ERR_INVALID_ARG;
+    if (mode == 1 && s->n_committed + F > kMaxFrames) return SR_ERR_STATE;
+    packed += s->lq;
+  }
+  if (packed > (int64_t(1) << 28)) return SR_ERR_INVALID_ARG;
+
+  auto* p = new (std::nothrow) sr::LayerRopeParams;
+  if (!p) return SR_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  p->phase = a->phase;
+  p->src[0] = static_cast<const __nv_bfloat16*>(s0);
+  p->src[1] = static_cast<const __nv_bfloat16*>(s1);
+  p->src[2] = static_cast<const __nv_bfloat16*>(s2);
+  p->dst[0] = static_cast<__nv_bfloat16*>(d0);
+  p->dst[1] = static_cast<__nv_bfloat16*>(d1);
+  p->dst[2] = static_cast<__nv_bfloat16*>(d2);
+  p->frame_h = fh;
+  p->frame_w = fw;
+  p->n_heads = a->cfg.n_heads;
+  p->t_clock0 = a->cfg.t_clock0;
+  p->mode = mode;
+  p->tokens_per_cta = sr::layer_tokens_per_cta(a->cfg.n_heads, a->cfg.head_dim);
+  int64_t ctas = 0, row = 0;
+  int nw = 0;
+  for (int i = 0; i < n; ++i) {
+    const sr_session* s = ss[i];
+    const int64_t W = s->cfg.window_frames;
+    const int64_t first = (mode == 1 && F > W) ? F - W : 0;   // a commit keeps the chunk's last W frames
+    const int64_t ntok = (mode == 1 && W == 0) ? 0 : (F - first) * s->tokens_per_frame;
+    if (ntok > 0) {
+      sr::LayerWindow& lw = p->win[nw++];
+      lw.row0 = wins[i].row0;
+      lw.col0 = wins[i].col0;
+      lw.rows = wins[i].rows;
+      lw.cols = wins[i].cols;
+      lw.packed_row0 = row;
+      lw.n_committed = s->n_committed;
+      lw.ring_k = static_cast<__nv_bfloat16*>(s->buf.ring_k);
+      lw.ring_v = static_cast<__nv_bfloat16*>(s->buf.ring_v);
+      lw.slot_frame = s->buf.slot_frame;
+      lw.window_frames = static_cast<int32_t>(W);
+      lw.first_frame = static_cast<int32_t>(first);
+      lw.cta_begin = static_cast<int32_t>(ctas);
+      lw.n_tok = static_cast<int32_t>(ntok);
+      ctas += (ntok + p->tokens_per_cta - 1) / p->tokens_per_cta;
+    }
+    row += s->lq;
+  }
+  p->n_windows = nw;
+  sr_status st = SR_OK;
+  if (ctas > (int64_t(1) << 30)) st = SR_ERR_INVALID_ARG;
+  if (st == SR_OK && nw > 0 &&
+      sr::launch_layer_rope(*p, a->cfg.head_dim, static_cast<int>(ctas), static_cast<cudaStream_t>(stream)) !=
+          cudaSuccess)
+    st = SR_ERR_CUDA;
+  delete p;
+  if (st == SR_OK && mode == 1)
+    for (int i = 0; i < n; ++i) ss[i]->n_committed += F;
+  return st;
+}
+
+sr_status sr_layer_rope_gather(sr_session* const* sessions, const sr_window* windows, int32_t n, int32_t frame_h,
+                               int32_t frame_w, const void* q, const void* k, const void* v, void* q_packed,
+                               void* k_packed, void* v_packed, void* stream) {
+  return layer_common(sessions, windows, n, frame_h, frame_w, q, k, v, q_packed, k_packed, v_packed, 0, stream);
+}
+
+sr_status sr_layer_commit(sr_session* const* sessions, const sr_window* windows, int32_t n, int32_t frame_h,
+                          int32_t frame_w, const void* k_raw, const void* v, void* stream) {
+  return layer_common(sessions, windows, n, frame_h, frame_w, k_raw, v, nullptr, nullptr, nullptr, nullptr, 1,
+                      stream);
+}
+
 // The unit rhythm of the teardown's shipped configuration: latents come in
 // codec groups of five (the first covers one RGB frame, the others four);
 // merging that one-frame latent into its neighbour makes units of 2, 1, 1, 1

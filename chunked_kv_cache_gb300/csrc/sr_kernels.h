@@ -171,6 +171,37 @@ struct RopeParams {
 
 cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st);
 
+// A decoder layer's windows in one launch: gather from frame-major tensors
+// [F][frame_h][frame_w][H][d] into the window-packed layout with RoPE at
+// window-relative (h, w) (mode 0), or write every window's ring slots (mode 1).
+constexpr int kMaxLayerWindows = SR_MAX_LAYER_WINDOWS;
+struct LayerWindow {
+  int32_t row0, col0, rows, cols;   // the window in the frame
+  int64_t packed_row0;              // mode 0: first packed row of the window
+  int64_t n_committed;              // frames the window's session committed before this chunk
+  __nv_bfloat16* ring_k;            // mode 1: the window's ring [W*rows*cols][H][d]
+  __nv_bfloat16* ring_v;
+  int32_t* slot_frame;              // mode 1: [W]
+  int32_t window_frames;            // mode 1: W
+  int32_t first_frame;              // first chunk frame processed (mode 1: F - W when F > W, else 0)
+  int32_t cta_begin;                // first CTA of this window
+  int32_t n_tok;                    // tokens processed
+};
+struct LayerRopeParams {
+  RopePhase phase;
+  const __nv_bfloat16* src[3];      // frame-major: q, k, v (mode 0) or k_raw, v (mode 1); v may be NULL in mode 0
+  __nv_bfloat16* dst[3];            // mode 0: packed q, k, v
+  int32_t frame_h, frame_w;
+  int32_t n_heads;
+  int32_t t_clock0;
+  int32_t mode;                     // 0: gather + rotate q, k (+ copy v); 1: commit k (rotated) and v
+  int32_t n_windows;
+  int32_t tokens_per_cta;
+  LayerWindow win[kMaxLayerWindows];
+};
+cudaError_t launch_layer_rope(const LayerRopeParams& p, int head_dim, int n_ctas, cudaStream_t st);
+int layer_tokens_per_cta(int n_heads, int head_dim);
+
 // ------------------------------------------------------------ misc
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);
 cudaError_t launch_init_ring_state(int32_t* slot_frame, int W, int32_t* err_word, int32_t* ws_ctr, int n_ctr,

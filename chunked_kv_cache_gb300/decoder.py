@@ -1,28 +1,37 @@
 """The streaming decoder's window attention on this library (host-side orchestration).
 
 [H3 page] "Interactive Coding Worlds with Real-time Streaming Diffusion Render",
-section 3.2 Iterations 2-4: each latent frame's tokens are cut into windows of
+section 3.2 Iterations 2-6: each latent frame's tokens are cut into windows of
 16x16 tokens (shifted by half a window on alternate layers); a window's chunk
 tokens attend to the global tokens, the window's cached frames and its own
 chunk frames, with positions relative to the window; the cache of each window
-is a preallocated ring written in place.
+is a preallocated ring written in place; the window gather is fused with the
+rotary embedding, and the rotary embedding with the cache write.
 
 Here every window is one session of the C library (grid = the window's size,
-F = chunk frames, W = cached frames), all sessions of a layer share one bank
-buffer holding the global tokens' keys and values (rewritten by the caller per
-chunk), and a layer's attention is the batched call over its windows, at most
-SR_MAX_BATCH windows per launch. Inputs come packed window by window, frame by
-frame, row-major inside the window (the variable-length layout: no padding);
-``packing_index`` gives the token permutation from whole frames to that layout.
-Nothing here computes: the rotary positions, the attention and the cache writes
-run in libsr.so.
+F = chunk frames, W = cached frames), and all sessions of a layer share one
+bank buffer holding the global tokens' keys and values (rewritten by the
+caller per chunk). A layer takes three kinds of launch, each covering every
+window (up to SR_MAX_LAYER_WINDOWS, resp. SR_MAX_BATCH for the attention):
+
+* ``gather_rope``: frame-major Q, K, V [F][grid_h][grid_w][H][d] -> the
+  window-packed layout (window by window, frame by frame, row-major inside
+  the window; no padding), Q and K rotated at window-relative positions;
+* ``attention``: the batched attention of every window over its visible set;
+* ``commit``: every window's frames of the clean K (rotated) and V into the
+  window's ring.
+
+``packing_index`` gives the token permutation from whole frames to the packed
+layout (to scatter packed outputs back). Nothing here computes: the gather,
+the rotary positions, the attention and the cache writes run in libsr.so.
 """
 from __future__ import annotations
 
 import torch
 
-from . import Session, chunk_attention_batch
-from ._native import SR_MAX_BATCH, sr_plan_window, sr_window_count
+from . import Session, _ptr, _stream, chunk_attention_batch
+from ._native import (SR_MAX_BATCH, SR_MAX_LAYER_WINDOWS, sr_layer_commit, sr_layer_rope_gather, sr_plan_window,
+                      sr_window_count)
 
 
 class DecoderWindowLayer:
@@ -43,8 +52,10 @@ class DecoderWindowLayer:
         self.offsets = [0]
         for s in self.sessions:
             self.offsets.append(self.offsets[-1] + s.lq)
-        # groups of windows per launch, each a contiguous row range of the packed layout
+        # groups of windows per attention launch, each a contiguous row range of the packed layout
         self.groups = [range(i, min(i + SR_MAX_BATCH, n)) for i in range(0, n, SR_MAX_BATCH)]
+        # groups of windows per gather / commit launch
+        self.layer_groups = [range(i, min(i + SR_MAX_LAYER_WINDOWS, n)) for i in range(0, n, SR_MAX_LAYER_WINDOWS)]
 
     @property
     def rows(self) -> int:
@@ -61,21 +72,45 @@ class DecoderWindowLayer:
             idx.append(((f * self.gh + r) * self.gw + c).reshape(-1))
         return torch.cat(idx)
 
-    def _slices(self, t: torch.Tensor, i: int) -> torch.Tensor:
-        return t[self.offsets[i]:self.offsets[i + 1]]
+    def _frames(self, name: str, t: torch.Tensor) -> None:
+        ok = (t.dtype == torch.bfloat16 and t.device == self.device and t.is_contiguous()
+              and t.numel() == self.F * self.gh * self.gw * self.H * self.d)
+        if not ok:
+            raise ValueError(f"{name}: expected a contiguous bf16 [F][grid_h][grid_w][H][d] tensor on {self.device}")
+
+    def _packed(self, name: str, t: torch.Tensor) -> None:
+        if t.dtype != torch.bfloat16 or t.device != self.device or not t.is_contiguous() or \
+                tuple(t.shape) != (self.rows, self.H, self.d):
+            raise ValueError(f"{name}: expected a contiguous bf16 [{self.rows}][{self.H}][{self.d}] tensor")
 
     def set_global(self, k: torch.Tensor, v: torch.Tensor) -> None:
         """The chunk's global-token keys and values, [G][H][d] (final, no rotation)."""
         self.bank_k[0].copy_(k)
         self.bank_v[0].copy_(v)
 
-    def rope(self, q: torch.Tensor, k: torch.Tensor) -> None:
-        """Rotary positions (relative to each window, absolute frame time) on packed q, k."""
-        for i, s in enumerate(self.sessions):
-            s.rope3d_qk(self._slices(q, i), self._slices(k, i))
+    def gather_rope(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor | None = None,
+                    out: tuple | None = None):
+        """Frame-major q, k (and v) -> packed (q, k, v): q and k rotated at
+        window-relative (h, w) and absolute frame time, v copied (None: not
+        gathered, returned as None). One launch per SR_MAX_LAYER_WINDOWS windows."""
+        for name, t in (("q", q), ("k", k)) + ((("v", v),) if v is not None else ()):
+            self._frames(name, t)
+        if out is None:
+            out = tuple(torch.empty((self.rows, self.H, self.d), dtype=torch.bfloat16, device=self.device)
+                        if t is not None else None for t in (q, k, v))
+        for name, t in zip(("q_out", "k_out", "v_out"), out):
+            if t is not None:
+                self._packed(name, t)
+        qo, ko, vo = out
+        for g in self.layer_groups:
+            row = self.offsets[g.start]
+            at = lambda t: 0 if t is None else t[row:].data_ptr()
+            sr_layer_rope_gather([self.sessions[i].handle for i in g], [self.windows[i] for i in g], self.gh, self.gw,
+                                 q.data_ptr(), k.data_ptr(), _ptr(v), at(qo), at(ko), at(vo), _stream(self.device))
+        return qo, ko, vo
 
     def attention(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None):
-        """Every window's chunk rows over global tokens U its cached frames U its chunk."""
+        """Every window's chunk rows (packed) over global tokens U its cached frames U its chunk."""
         if out is None:
             out = torch.empty_like(q)
         for g in self.groups:
@@ -84,9 +119,13 @@ class DecoderWindowLayer:
         return out
 
     def commit(self, k: torch.Tensor, v: torch.Tensor) -> None:
-        """Write the chunk's frames into every window's cache ring (K rotated at its frames)."""
-        for i, s in enumerate(self.sessions):
-            s.cache_commit(self._slices(k, i), self._slices(v, i))
+        """Write the chunk's frames (frame-major clean K and V) into every window's
+        cache ring, K rotated at its frames. One launch per SR_MAX_LAYER_WINDOWS windows."""
+        self._frames("k", k)
+        self._frames("v", v)
+        for g in self.layer_groups:
+            sr_layer_commit([self.sessions[i].handle for i in g], [self.windows[i] for i in g], self.gh, self.gw,
+                            k.data_ptr(), v.data_ptr(), _stream(self.device))
 
     def error_status(self) -> int:
         return max(abs(s.error_status()) for s in self.sessions)

@@ -381,6 +381,34 @@ SR_API sr_status sr_plan_window(int32_t grid_h, int32_t grid_w, int32_t window, 
  */
 SR_API sr_status sr_rope_angle(const sr_config* cfg, int32_t pair, int64_t position, float* angle);
 
+/*
+ * A decoder layer's rotary positions, window gather and cache writes, one launch each
+ * ([H3 page] 3.2 Iteration 3: the window gather is fused with the rotary embedding;
+ * Iteration 6: rotary positions and the K/V cache write in one kernel; Iteration 2
+ * "Space": positions relative to the window).
+ * sessions[i] is the session of window windows[i] of a frame_h x frame_w latent frame
+ * (its grid must be windows[i].rows x windows[i].cols, e.g. from sr_plan_window); all
+ * sessions share n_heads, head_dim, chunk_frames F, t_clock0 and rope_base.
+ * 1 <= n <= SR_MAX_LAYER_WINDOWS. Frame-major tensors are [F][frame_h][frame_w][H][d]
+ * bf16; packed tensors hold the windows' rows back to back in the order of `sessions`
+ * (window i from row sum_{j<i} F*rows_j*cols_j; inside a window frame by frame,
+ * row-major), the layout sr_chunk_attention_batch reads.
+ * - sr_layer_rope_gather: q, k (frame-major) rotated at each window's frames n .. n+F-1
+ *   (time t_clock0 + n + f) and window-relative (h, w), written to q_packed, k_packed;
+ *   v (optional, NULL to skip) copied to v_packed. The frame-major inputs are not changed.
+ * - sr_layer_commit: as sr_cache_commit for every session at once: each window's frames
+ *   of k_raw (rotated as above) and v written into its ring slots, its slot table updated,
+ *   its n advanced by F.
+ * Validation failures (SR_ERR_INVALID_ARG, SR_ERR_ALIGN, SR_ERR_STATE as for the
+ * per-session calls) change nothing.
+ */
+#define SR_MAX_LAYER_WINDOWS 96
+SR_API sr_status sr_layer_rope_gather(sr_session* const* sessions, const sr_window* windows, int32_t n,
+                                      int32_t frame_h, int32_t frame_w, const void* q, const void* k,
+                                      const void* v, void* q_packed, void* k_packed, void* v_packed, void* stream);
+SR_API sr_status sr_layer_commit(sr_session* const* sessions, const sr_window* windows, int32_t n,
+                                 int32_t frame_h, int32_t frame_w, const void* k_raw, const void* v, void* stream);
+
 /* Map a value read from err_word to SR_OK or SR_ERR_TIMEOUT. */
 SR_API sr_status sr_device_error_status(int32_t err_word_value);
 

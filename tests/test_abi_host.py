@@ -121,6 +121,27 @@ def test_null_arguments(lib):
     assert L.sr_chunk_attention_batch(arr, 17, 0, 16, 16, 16, offs, 16, None, None) == N.SR_ERR_INVALID_ARG
 
 
+def test_layer_calls_reject_bad_arguments(lib):
+    L = N.lib()
+    arr = (ctypes.c_void_p * 1)(None)
+    wins = (N.SrWindow * 1)(N.SrWindow(0, 0, 16, 16))
+    # NULL sessions / windows, a NULL session inside, n out of range, empty frame
+    assert L.sr_layer_rope_gather(None, wins, 1, 16, 16, 16, 16, None, 16, 16, None, None) == N.SR_ERR_INVALID_ARG
+    assert L.sr_layer_rope_gather(arr, None, 1, 16, 16, 16, 16, None, 16, 16, None, None) == N.SR_ERR_INVALID_ARG
+    assert L.sr_layer_rope_gather(arr, wins, 1, 16, 16, 16, 16, None, 16, 16, None, None) == N.SR_ERR_INVALID_ARG
+    assert L.sr_layer_rope_gather(arr, wins, 0, 16, 16, 16, 16, None, 16, 16, None, None) == N.SR_ERR_INVALID_ARG
+    assert L.sr_layer_rope_gather(arr, wins, N.SR_MAX_LAYER_WINDOWS + 1, 16, 16, 16, 16, None, 16, 16, None,
+                                  None) == N.SR_ERR_INVALID_ARG
+    assert L.sr_layer_rope_gather(arr, wins, 1, 0, 16, 16, 16, None, 16, 16, None, None) == N.SR_ERR_INVALID_ARG
+    # v without v_packed
+    assert L.sr_layer_rope_gather(arr, wins, 1, 16, 16, 16, 16, 16, 16, 16, None, None) == N.SR_ERR_INVALID_ARG
+    # a misaligned pointer is refused before the sessions are looked at
+    assert L.sr_layer_rope_gather(arr, wins, 1, 16, 16, 24, 16, None, 16, 16, None, None) == N.SR_ERR_ALIGN
+    assert L.sr_layer_commit(None, wins, 1, 16, 16, 16, 16, None) == N.SR_ERR_INVALID_ARG
+    assert L.sr_layer_commit(arr, wins, 1, 16, 16, None, 16, None) == N.SR_ERR_INVALID_ARG
+    assert L.sr_layer_commit(arr, wins, 1, 16, 16, 16, 8, None) == N.SR_ERR_ALIGN
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(N, "_lib", None)
     monkeypatch.setattr(N, "LIB_PATH", str(tmp_path / "libsr.so"))

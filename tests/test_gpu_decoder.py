@@ -12,7 +12,8 @@ import torch
 
 import synthetic as syn
 from oracle.decoder import DecoderLayerOracle
-from tests.gpu_common import assert_attention_close, device
+from oracle import f64_to_bf16_bits
+from tests.gpu_common import assert_attention_close, assert_rotated_close, device
 
 pytestmark = pytest.mark.gpu
 
@@ -31,30 +32,88 @@ def _bits_dev(bits, dev):
 @pytest.mark.parametrize("gh,gw,H,d", [(40, 40, 4, 64), (21, 37, 2, 128)])
 @pytest.mark.parametrize("shifted", [False, True])
 def test_decoder_layer_stream(gh, gw, H, d, shifted):
+    """Frame-major inputs through the layer calls: one gather + RoPE launch, one
+    batched attention launch, one commit launch per chunk."""
     from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
     dev = device()
     G, F = 5, 2
     lay = DecoderWindowLayer(gh, gw, H, d, G, shifted=shifted, t_clock0=4, device=dev)
     ora = DecoderLayerOracle(gh, gw, 16, shifted, H, d, cache_frames=4, t_clock0=4)
     assert [(w.row0, w.col0, w.rows, w.cols) for w in lay.windows] == ora.windows
-    idx = lay.packing_index().to(dev)
+    idx = lay.packing_index().numpy()
     rng = np.random.default_rng(gh + shifted)
     for c in range(4):
         q, k, v, ck, cv = (syn.normal_bf16_bits((F, gh, gw, H, d), rng) for _ in range(5))
         gk, gv = syn.normal_bf16_bits((G, H, d), rng), syn.normal_bf16_bits((G, H, d), rng)
-        pk = lambda b: _bits_dev(b, dev).reshape(F * gh * gw, H, d)[idx].contiguous()
-        qd, kd, vd, ckd, cvd = pk(q), pk(k), pk(v), pk(ck), pk(cv)
+        qd, kd, vd, ckd, cvd = (_bits_dev(b, dev) for b in (q, k, v, ck, cv))
         lay.set_global(_bits_dev(gk, dev), _bits_dev(gv, dev))
-        lay.rope(qd, kd)
-        o = lay.attention(qd, kd, vd)
+        qp, kp, vp = lay.gather_rope(qd, kd, vd)
+        o = lay.attention(qp, kp, vp)
         lay.commit(ckd, cvd)
         ref = ora.step(q, k, v, gk, gv)
         ora.commit(ck, cv)
         got = np.empty((F * gh * gw, H, d))
-        got[idx.cpu().numpy()] = o.float().cpu().numpy()
+        got[idx] = o.float().cpu().numpy()
         assert_attention_close(got, ref.reshape(-1, H, d), f"chunk {c} (cache {min(2 * c, 4)} frames)")
+        # the packed V is a plain gather of the frame-major V
+        assert np.array_equal(syn.torch_to_bits(vp), v.reshape(-1, H, d)[idx])
+    # every window's ring holds its cached frames: K rotated like the oracle's, V copied
+    for s, (r0, c0, nr, nc) in zip(lay.sessions, ora.windows):
+        rk, rv = syn.torch_to_bits(s.ring_k), syn.torch_to_bits(s.ring_v)
+        slots = s.slot_frame.cpu().numpy()
+        T = nr * nc
+        for g, ok_, ov_ in ora.cache:
+            slot = g % 4
+            assert slots[slot] == g
+            want_k = f64_to_bf16_bits(ok_[r0:r0 + nr, c0:c0 + nc]).reshape(T, H, d)
+            want_v = f64_to_bf16_bits(ov_[r0:r0 + nr, c0:c0 + nc]).reshape(T, H, d)
+            assert np.array_equal(rv[slot * T:(slot + 1) * T], want_v)
+            assert_rotated_close(rk[slot * T:(slot + 1) * T], want_k, f"ring K of window ({r0}, {c0}) frame {g}")
     assert lay.error_status() == 0
     lay.close()
+
+
+def test_layer_calls_match_per_window_calls_bit_for_bit():
+    """The one-launch gather + RoPE and commit of a layer give the same bits as
+    the per-window calls on a gather done by indexing (the same arithmetic)."""
+    import chunked_kv_cache_gb300 as sr
+    from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
+    dev = device()
+    gh, gw, H, d, G, F = 45, 80, 3, 128, 5, 2
+    for shifted in (False, True):
+        lay = DecoderWindowLayer(gh, gw, H, d, G, shifted=shifted, t_clock0=9, device=dev)
+        ref = DecoderWindowLayer(gh, gw, H, d, G, shifted=shifted, t_clock0=9, device=dev)
+        idx = lay.packing_index().to(dev)
+        rng = np.random.default_rng(40 + shifted)
+        for c in range(3):   # 6 frames through 4-frame rings: the commits wrap
+            q, k, v, ck, cv = (_bits_dev(syn.normal_bf16_bits((F, gh, gw, H, d), rng), dev) for _ in range(5))
+            qp, kp, vp = lay.gather_rope(q, k, v)
+            flat = lambda t: t.reshape(F * gh * gw, H, d)[idx].contiguous()
+            rq, rk_, rv = flat(q), flat(k), flat(v)
+            for i, s in enumerate(ref.sessions):
+                a, b = ref.offsets[i], ref.offsets[i + 1]
+                s.rope3d_qk(rq[a:b], rk_[a:b])
+            assert torch.equal(qp, rq) and torch.equal(kp, rk_) and torch.equal(vp, rv)
+            lay.commit(ck, cv)
+            pck, pcv = flat(ck), flat(cv)
+            for i, s in enumerate(ref.sessions):
+                a, b = ref.offsets[i], ref.offsets[i + 1]
+                s.cache_commit(pck[a:b], pcv[a:b])
+            torch.cuda.synchronize()
+            for s1, s2 in zip(lay.sessions, ref.sessions):
+                assert s1.frames == s2.frames == F * (c + 1)
+                assert torch.equal(s1.slot_frame, s2.slot_frame)
+                # the slots written so far (the others hold whatever the allocator left)
+                rows = torch.repeat_interleave(s1.slot_frame >= 0, s1.T)
+                assert torch.equal(s1.ring_k[rows], s2.ring_k[rows]) and torch.equal(s1.ring_v[rows], s2.ring_v[rows])
+        # only the packed rows were written: the frame-major inputs are untouched
+        q0 = _bits_dev(syn.normal_bf16_bits((F, gh, gw, H, d), rng), dev)
+        keep = q0.clone()
+        lay.gather_rope(q0, q0.clone())
+        assert torch.equal(q0, keep)
+        assert lay.error_status() == 0 and ref.error_status() == 0
+        lay.close()
+        ref.close()
 
 
 def test_decoder_layer_graph_replay_matches_eager():
