@@ -140,8 +140,6 @@ struct SmemBars {
   uint64_t x_empty;       // split mode: group 0 has read them and both O accumulators
   uint64_t part_done;     // key split: group 0's partial rows are published
   uint64_t part_last;     // key split: `last` is set
-  uint64_t o_staged[2];   // group t's rows of one O atom are in its staging buffer
-  uint64_t o_free[2];     // group t's staging buffer has been read by its tile store
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -399,10 +397,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     mbar_init(&bars->x_empty, BM);
     mbar_init(&bars->part_done, BM);
     mbar_init(&bars->part_last, 1);
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->o_staged[t], BM);
-      mbar_init(&bars->o_free[t], 1);
-    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -758,7 +752,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     uint32_t od0 = 0, od1 = 0;   // o_done completions of each tile so far
     uint32_t nx = 0;             // split-mode units so far
     uint32_t nk = 0;             // key-split units so far
-    uint32_t ns = 0;             // O atoms this group has sent through its staging buffer
     while (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[uk % kUnitSlots], (uk / kUnitSlots) & 1, wc, 8));
       if (!ok) break;
@@ -882,13 +875,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         if (ok && merge) ok = wait_bounded(&bars->o_done[1], w1 & 1u, wc, 6);
         ok = __all_sync(0xffffffffu, ok);
       }
-      // A whole 128-row tile of a shared-mode unit leaves through tile stores,
-      // one 64-column atom at a time, staged in this group's half of the K/V
-      // stage that shared mode leaves unused (D = 128): coalesced and off the
-      // load/store pipe. Not when the next unit is a split-mode one, whose
-      // third stage pair lives there (its record is out long before this).
+      // The output rows of a shared-mode unit leave through shared memory, one
+      // 64-column atom at a time: each warp writes its 32 rows into its 4 KB of
+      // the K/V stage that shared mode leaves unused (D = 128), reads them back
+      // four rows per instruction and stores them so that every 128-byte row
+      // segment is written whole by 8 lanes. No barrier beyond the warp and no
+      // copy engine: a tile store through the tensor-memory-access unit queued
+      // behind the next unit's loads, and its round trips (staging barrier,
+      // store, wait for the read) took 3 us of a 23 us decoder unit. Not when
+      // the next unit is a split-mode one, whose third stage pair lives in that
+      // stage (its record is out long before this).
       bool staged = false;
-      if (D == 128 && ok && !wk.split && parts == 1 && r.q_local0 + (t + 1) * BM <= S.lq) {
+      if (D == 128 && ok && !wk.split && parts == 1 && r.q_local0 + t * BM < S.lq) {
         const int kn = uk + 1;
         ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[kn % kUnitSlots], (kn / kUnitSlots) & 1, wc, 11));
         const UnitRec& rn = bars->rec[kn % kUnitSlots];
@@ -914,40 +912,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
         const uint32_t t_o1 = tmem + lane_base + 256 + 128;
         if (staged) {
-          // [128 rows][64 cols] bf16 with the 128-byte swizzle of the tile map:
-          // 16-byte chunk j of row r at r * 128 + ((j ^ (r % 8)) * 16)
-          uint8_t* buf = sKV + 4 * C::kTileBytes + t * C::kAtomBytes;
+          // 16-byte chunk j of the warp's row rr at rr * 128 + ((j ^ (rr % 8)) * 16):
+          // the writes of 8 lanes and the reads of 8 lanes each cover every bank once
+          uint8_t* wbuf = sKV + 4 * C::kTileBytes + t * C::kAtomBytes + (warp % 4) * 32 * 128;
+          // this lane stores chunk (lane % 8) of rows lane / 8, lane / 8 + 4, ... of the warp's 32
+          const int live = S.lq - (r.q_local0 + t * BM) - (warp % 4) * 32 - lane / 8;   // > 4i: row 4i + lane/8 is live
+          const int64_t grow = static_cast<int64_t>(S.q_row0) + r.q_local0 + t * BM + (warp % 4) * 32 + lane / 8;
+          __nv_bfloat16* orow = p.o + (grow * p.n_heads + head) * D + (lane % 8) * 8;
+          const int64_t ostride = static_cast<int64_t>(4) * p.n_heads * D;   // four rows
 #pragma unroll 1
-          for (int a = 0; a < 2 && ok; ++a) {
-            // the atom's 64 columns, normalised and packed, before the buffer wait
-            uint4 pkt[8];
+          for (int a = 0; a < 2; ++a) {
+            __syncwarp();   // the previous atom's reads of the buffer are done
+            // the atom's 64 columns of this thread's row, normalised and packed,
+            // 32 columns (four 16-byte chunks) at a time
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
               uint32_t o[32];
               tmem_ld32(t_o + (a * 2 + c2) * 32, o);
               tmem_wait_ld();
               tmem_fix(o);
-              uint32_t* w = reinterpret_cast<uint32_t*>(&pkt[c2 * 4]);
+              uint4 pkt[4];
+              uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
 #pragma unroll
               for (int i = 0; i < 16; ++i)
                 w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f0, __uint_as_float(o[2 * i + 1]) * f0);
-            }
-            if (ns > 0) ok = __all_sync(0xffffffffu, wait_bounded(&bars->o_free[t], (ns - 1) & 1u, wc, 12));
-            if (!ok) break;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(buf + row * 128 + ((j ^ (row & 7)) * 16)) = pkt[j];
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->o_staged[t]);
-            if (row == 0) {   // the group's first thread sends the atom
-              if (wait_bounded(&bars->o_staged[t], ns & 1u, wc, 13)) {
-                tma_store_2d(&p.omap, buf, head * D + a * 64, S.q_row0 + r.q_local0 + t * BM);
-                bulk_commit_group();
-                bulk_wait_read_all();
-              }
-              mbar_arrive(&bars->o_free[t]);
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(wbuf + lane * 128 + (((c2 * 4 + j) ^ (lane & 7)) * 16)) = pkt[j];
             }
-            ++ns;
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = i * 4 + lane / 8;   // row within the warp's 32
+              const uint4 v = *reinterpret_cast<const uint4*>(wbuf + rr * 128 + (((lane % 8) ^ (rr & 7)) * 16));
+              if (4 * i < live) *reinterpret_cast<uint4*>(orow + i * ostride + a * 64) = v;
+            }
           }
+          __syncwarp();
+          fence_proxy_async_smem();   // the stage may next be filled by a tensor copy
         }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -1031,9 +1033,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
   }
 
-  // shared memory outlives every tile store's read of it (the stores' writes
-  // complete with the grid)
-  if (warp < 8 && threadIdx.x % BM == 0) bulk_wait_read_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

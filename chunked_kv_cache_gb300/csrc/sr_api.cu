@@ -511,7 +511,7 @@ sr_status attention_into_scratch(sr_session* s, int32_t step, const void* q, con
   AttnParams<1> p;                                  // on the stack: nothing is allocated
   std::memset(&p, 0, sizeof(p));
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
-  if (!encode_cached(s, &p.qmap, q, s->lq, row_elems) || !encode_cached(s, &p.omap, o, s->lq, row_elems))
+  if (!encode_cached(s, &p.qmap, q, s->lq, row_elems))
     return SR_ERR_CUDA;
   // the scratch stands in for the session's workspace for this call only
   void* own = s->buf.workspace;
@@ -763,7 +763,7 @@ static sr_status attention_view(sr_session* s, const ChunkView& view, int32_t st
   std::memset(p, 0, sizeof(*p));
   const int64_t row_elems = static_cast<int64_t>(s->cfg.n_heads) * s->cfg.head_dim;
   sr_status st = SR_OK;
-  if (!encode_cached(s, &p->qmap, q, view.lq, row_elems) || !encode_cached(s, &p->omap, o, view.lq, row_elems))
+  if (!encode_cached(s, &p->qmap, q, view.lq, row_elems))
     st = SR_ERR_CUDA;
   if (st == SR_OK) st = fill_session(p->sess[0], s, view, step, k, v, 0);
   int n_units = 0;
@@ -865,7 +865,7 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
   if (!p) return SR_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   sr_status st = SR_OK;
-  if (!encode_cached(s, &p->qmap, q, P + M, row_elems) || !encode_cached(s, &p->omap, o, P + M, row_elems))
+  if (!encode_cached(s, &p->qmap, q, P + M, row_elems))
     st = SR_ERR_CUDA;
   // Two query groups in one launch. Moving rows (longest key range first):
   // the bank of the step and the moving rows themselves. Prefix rows: the
@@ -949,8 +949,7 @@ sr_status sr_chunk_attention_batch(sr_session* const* sessions, int32_t n, int32
   std::memset(p, 0, sizeof(*p));
   const int64_t row_elems = static_cast<int64_t>(s0->cfg.n_heads) * s0->cfg.head_dim;
   sr_status st = SR_OK;
-  if (!encode_cached(sessions[order[0]], &p->qmap, q, total, row_elems) ||
-      !encode_cached(sessions[order[0]], &p->omap, o, total, row_elems))
+  if (!encode_cached(sessions[order[0]], &p->qmap, q, total, row_elems))
     st = SR_ERR_CUDA;
   // units: every session's whole 256-row blocks (sessions by decreasing key
   // count), then the single-tile last blocks -- longest work first

@@ -79,7 +79,6 @@ struct alignas(128) AttnSession {
 template <int NSESS>
 struct alignas(128) AttnParams {
   CUtensorMap qmap;               // packed q, [total_rows][H*d]
-  CUtensorMap omap;               // packed o, [total_rows][H*d] (tile stores of whole output tiles)
   AttnSession sess[NSESS];
   int32_t n_sess;
   int32_t n_full_units;           // whole 256-row blocks (all sessions); last blocks follow
