@@ -225,6 +225,48 @@ __device__ __noinline__ void merge_key_parts(const float* __restrict__ hbase, in
   }
 }
 
+// The output rows of one 128-row tile of a shared-mode unit, one 64-column
+// atom at a time through this warp's 4 KB of shared memory (16-byte chunk j of
+// the warp's row rr at rr * 128 + ((j ^ (rr % 8)) * 16), so neither the writes
+// nor the reads conflict on banks): each thread writes its row's atom, then
+// each lane reads chunk lane % 8 of rows lane / 8, lane / 8 + 4, ... and stores
+// it, so that 8 lanes write each 128-byte row segment whole. orow: this lane's
+// first row and chunk in global memory; ostride: four rows; live: the lane's
+// rows 4i + lane / 8 with 4i < live belong to the session. Out of line: it runs
+// once per unit and keeps its registers out of the softmax loop's allocation.
+template <int D>
+__device__ __noinline__ void store_rows_staged(uint32_t t_o, float f0, uint8_t* wbuf, __nv_bfloat16* orow,
+                                               int64_t ostride, int live, int lane) {
+#pragma unroll 1
+  for (int a = 0; a < D / 64; ++a) {
+    __syncwarp();   // the previous atom's reads of the buffer are done
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+      uint32_t o[32];
+      tmem_ld32(t_o + (a * 2 + c2) * 32, o);
+      tmem_wait_ld();
+      tmem_fix(o);
+      uint4 pkt[4];
+      uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f0, __uint_as_float(o[2 * i + 1]) * f0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(wbuf + lane * 128 + (((c2 * 4 + j) ^ (lane & 7)) * 16)) = pkt[j];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + lane / 8;
+      const uint4 v = *reinterpret_cast<const uint4*>(wbuf + rr * 128 + (((lane % 8) ^ (rr & 7)) * 16));
+      if (4 * i < live) *reinterpret_cast<uint4*>(orow + i * ostride + a * 64) = v;
+    }
+  }
+  __syncwarp();
+  fence_proxy_async_smem();   // the stage may next be filled by a tensor copy
+}
+
 // The key tiles each query tile walks, within the unit's range [lo, lo + n) of
 // all key tiles: in shared mode both walk the whole range; in split mode tile 0
 // walks [lo, lo + h) and tile 1 walks [lo + h, lo + n).
@@ -912,44 +954,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
         const uint32_t t_o1 = tmem + lane_base + 256 + 128;
         if (staged) {
-          // 16-byte chunk j of the warp's row rr at rr * 128 + ((j ^ (rr % 8)) * 16):
-          // the writes of 8 lanes and the reads of 8 lanes each cover every bank once
-          uint8_t* wbuf = sKV + 4 * C::kTileBytes + t * C::kAtomBytes + (warp % 4) * 32 * 128;
-          // this lane stores chunk (lane % 8) of rows lane / 8, lane / 8 + 4, ... of the warp's 32
-          const int live = S.lq - (r.q_local0 + t * BM) - (warp % 4) * 32 - lane / 8;   // > 4i: row 4i + lane/8 is live
+          const int live = S.lq - (r.q_local0 + t * BM) - (warp % 4) * 32 - lane / 8;
           const int64_t grow = static_cast<int64_t>(S.q_row0) + r.q_local0 + t * BM + (warp % 4) * 32 + lane / 8;
-          __nv_bfloat16* orow = p.o + (grow * p.n_heads + head) * D + (lane % 8) * 8;
-          const int64_t ostride = static_cast<int64_t>(4) * p.n_heads * D;   // four rows
-#pragma unroll 1
-          for (int a = 0; a < 2; ++a) {
-            __syncwarp();   // the previous atom's reads of the buffer are done
-            // the atom's 64 columns of this thread's row, normalised and packed,
-            // 32 columns (four 16-byte chunks) at a time
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-              uint32_t o[32];
-              tmem_ld32(t_o + (a * 2 + c2) * 32, o);
-              tmem_wait_ld();
-              tmem_fix(o);
-              uint4 pkt[4];
-              uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f0, __uint_as_float(o[2 * i + 1]) * f0);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4*>(wbuf + lane * 128 + (((c2 * 4 + j) ^ (lane & 7)) * 16)) = pkt[j];
-            }
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int rr = i * 4 + lane / 8;   // row within the warp's 32
-              const uint4 v = *reinterpret_cast<const uint4*>(wbuf + rr * 128 + (((lane % 8) ^ (rr & 7)) * 16));
-              if (4 * i < live) *reinterpret_cast<uint4*>(orow + i * ostride + a * 64) = v;
-            }
-          }
-          __syncwarp();
-          fence_proxy_async_smem();   // the stage may next be filled by a tensor copy
+          store_rows_staged<D>(t_o, f0, sKV + 4 * C::kTileBytes + t * C::kAtomBytes + (warp % 4) * 32 * 128,
+                               p.o + (grow * p.n_heads + head) * D + (lane % 8) * 8,
+                               static_cast<int64_t>(4) * p.n_heads * D, live, lane);
         }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
