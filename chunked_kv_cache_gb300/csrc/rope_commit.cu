@@ -187,8 +187,9 @@ cudaError_t launch_rope(const RopeParams& p, int head_dim, cudaStream_t st) {
 
 namespace {
 
-template <int D>
+template <int D, int VPT, bool kThird>
 __global__ void __launch_bounds__(kRopeThreads) layer_rope_kernel(const LayerRopeParams p) {
+  constexpr int kTarget = kRopeThreads * VPT;   // vectors of each tensor per pass
   constexpr int kPairs = D / 2;
   constexpr int kVecPerHead = D / 8;
   grid_dep_wait();   // the previous kernel of the stream may still be draining
@@ -243,25 +244,25 @@ __global__ void __launch_bounds__(kRopeThreads) layer_rope_kernel(const LayerRop
 
   const uint4* s0 = reinterpret_cast<const uint4*>(p.src[0]);
   const uint4* s1 = reinterpret_cast<const uint4*>(p.src[1]);
-  const uint4* s2 = reinterpret_cast<const uint4*>(p.src[2]);   // NULL: no third tensor
+  const uint4* s2 = reinterpret_cast<const uint4*>(p.src[2]);   // read only when kThird
   uint4* d0 = reinterpret_cast<uint4*>(commit ? p.win[wi].ring_k : p.dst[0]);
   uint4* d1 = reinterpret_cast<uint4*>(commit ? p.win[wi].ring_v : p.dst[1]);
   uint4* d2 = reinterpret_cast<uint4*>(p.dst[2]);
 
-  for (int base = 0; base < nvec; base += kRopeVecTarget) {
+  for (int base = 0; base < nvec; base += kTarget) {
     // loads first: they are in flight while the sin/cos table is built
-    uint4 a[kRopeVecPerThread], b[kRopeVecPerThread], c3[kRopeVecPerThread];
+    uint4 a[VPT], b[VPT], c3[kThird ? VPT : 1];
     {
       int j = base + threadIdx.x;
       int t = j / vpt;
       int r = j - t * vpt;
 #pragma unroll
-      for (int k = 0; k < kRopeVecPerThread; ++k) {
+      for (int k = 0; k < VPT; ++k) {
         if (j < nvec) {
           const int64_t at = src_row[t] * vpt + r;
           a[k] = s0[at];
           b[k] = s1[at];
-          if (s2 != nullptr) c3[k] = s2[at];
+          if constexpr (kThird) c3[k] = s2[at];
         }
         j += kRopeThreads;
         r += kRopeThreads;
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(kRopeThreads) layer_rope_kernel(const LayerRop
     int t = j / vpt;
     int r = j - t * vpt;
 #pragma unroll
-    for (int k = 0; k < kRopeVecPerThread; ++k) {
+    for (int k = 0; k < VPT; ++k) {
       if (j < nvec) {
         const float2* cs = cs_table + t * kPairs + (r & (kVecPerHead - 1)) * 4;
         uint32_t* wa = reinterpret_cast<uint32_t*>(&a[k]);
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kRopeThreads) layer_rope_kernel(const LayerRop
         const int64_t at = dst_row[t] * vpt + r;
         d0[at] = a[k];
         d1[at] = b[k];
-        if (s2 != nullptr) d2[at] = c3[k];
+        if constexpr (kThird) d2[at] = c3[k];
       }
       j += kRopeThreads;
       r += kRopeThreads;
@@ -322,27 +323,32 @@ size_t layer_smem_bytes(int tpc, int head_dim) {
 
 }  // namespace
 
-int layer_tokens_per_cta(int n_heads, int head_dim) {
-  return std::max(1, kRopeVecTarget / (n_heads * head_dim / 8));
+// 16-byte vectors of each tensor a thread keeps in flight: the gather moves
+// three tensors, the commit two, so the commit takes more per tensor.
+int layer_vec_per_thread(int mode) { return mode == 1 ? 6 : 4; }
+
+int layer_tokens_per_cta(int n_heads, int head_dim, int mode) {
+  return std::max(1, kRopeThreads * layer_vec_per_thread(mode) / (n_heads * head_dim / 8));
 }
+
+namespace {
+template <int D>
+cudaError_t launch_layer_d(const LayerRopeParams& p, int n_ctas, size_t smem, cudaStream_t st) {
+  // the commit (two tensors) keeps 6 vectors of each in flight, the gather 4 of its two or three
+  auto kernel = p.mode == 1 ? layer_rope_kernel<D, 6, false>
+                            : (p.src[2] != nullptr ? layer_rope_kernel<D, 4, true> : layer_rope_kernel<D, 4, false>);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_dependent(kernel, static_cast<unsigned>(n_ctas), kRopeThreads, smem, st, p);
+}
+}  // namespace
 
 cudaError_t launch_layer_rope(const LayerRopeParams& p, int head_dim, int n_ctas, cudaStream_t st) {
   if (n_ctas <= 0) return cudaSuccess;
   const size_t smem = layer_smem_bytes(p.tokens_per_cta, head_dim);
-  if (head_dim == 128) {
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(layer_rope_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-    }
-    return launch_dependent(layer_rope_kernel<128>, static_cast<unsigned>(n_ctas), kRopeThreads, smem, st, p);
-  }
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(layer_rope_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  return launch_dependent(layer_rope_kernel<64>, static_cast<unsigned>(n_ctas), kRopeThreads, smem, st, p);
+  return head_dim == 128 ? launch_layer_d<128>(p, n_ctas, smem, st) : launch_layer_d<64>(p, n_ctas, smem, st);
 }
 
 // ------------------------------------------------------------ small helpers

@@ -1031,7 +1031,7 @@ static sr_status layer_common(sr_session* const* ss, const sr_window* wins, int3
   p->n_heads = a->cfg.n_heads;
   p->t_clock0 = a->cfg.t_clock0;
   p->mode = mode;
-  p->tokens_per_cta = sr::layer_tokens_per_cta(a->cfg.n_heads, a->cfg.head_dim);
+  p->tokens_per_cta = sr::layer_tokens_per_cta(a->cfg.n_heads, a->cfg.head_dim, mode);
   int64_t ctas = 0, row = 0;
   int nw = 0;
   for (int i = 0; i < n; ++i) {

@@ -199,7 +199,7 @@ struct LayerRopeParams {
   LayerWindow win[kMaxLayerWindows];
 };
 cudaError_t launch_layer_rope(const LayerRopeParams& p, int head_dim, int n_ctas, cudaStream_t st);
-int layer_tokens_per_cta(int n_heads, int head_dim);
+int layer_tokens_per_cta(int n_heads, int head_dim, int mode);
 
 // ------------------------------------------------------------ misc
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);

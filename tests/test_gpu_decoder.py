@@ -116,6 +116,45 @@ def test_layer_calls_match_per_window_calls_bit_for_bit():
         ref.close()
 
 
+@pytest.mark.parametrize("gh,gw,window,F,C,d", [
+    (176, 176, 16, 2, 4, 64),    # 121 windows: two gather / commit launches of at most 96 windows
+    (20, 24, 8, 1, 3, 64),       # one-frame chunks into 3-frame caches (commits wrap every 3 chunks)
+    (16, 24, 8, 3, 0, 128),      # no cache: the commit only advances the frame counts
+])
+def test_layer_calls_edge_shapes_match_per_window_calls(gh, gw, window, F, C, d):
+    from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
+    dev = device()
+    H, G = 2, 5
+    lay = DecoderWindowLayer(gh, gw, H, d, G, window=window, chunk_frames=F, cache_frames=C, t_clock0=3, device=dev)
+    ref = DecoderWindowLayer(gh, gw, H, d, G, window=window, chunk_frames=F, cache_frames=C, t_clock0=3, device=dev)
+    idx = lay.packing_index().to(dev)
+    rng = np.random.default_rng(gh + F + C)
+    flat = lambda t: t.reshape(F * gh * gw, H, d)[idx].contiguous()
+    for c in range(4):
+        q, k, v, ck, cv = (_bits_dev(syn.normal_bf16_bits((F, gh, gw, H, d), rng), dev) for _ in range(5))
+        qp, kp, vp = lay.gather_rope(q, k, v)
+        rq, rk_, rv = flat(q), flat(k), flat(v)
+        for i, s in enumerate(ref.sessions):
+            a, b = ref.offsets[i], ref.offsets[i + 1]
+            s.rope3d_qk(rq[a:b], rk_[a:b])
+        assert torch.equal(qp, rq) and torch.equal(kp, rk_) and torch.equal(vp, rv), c
+        lay.commit(ck, cv)
+        pck, pcv = flat(ck), flat(cv)
+        for i, s in enumerate(ref.sessions):
+            a, b = ref.offsets[i], ref.offsets[i + 1]
+            s.cache_commit(pck[a:b], pcv[a:b])
+        torch.cuda.synchronize()
+        for s1, s2 in zip(lay.sessions, ref.sessions):
+            assert s1.frames == s2.frames == F * (c + 1)
+            if C > 0:
+                assert torch.equal(s1.slot_frame, s2.slot_frame)
+                rows = torch.repeat_interleave(s1.slot_frame >= 0, s1.T)
+                assert torch.equal(s1.ring_k[rows], s2.ring_k[rows]) and torch.equal(s1.ring_v[rows], s2.ring_v[rows])
+    assert lay.error_status() == 0 and ref.error_status() == 0
+    lay.close()
+    ref.close()
+
+
 def test_decoder_layer_graph_replay_matches_eager():
     """A layer's launches captured in a CUDA graph (persistent launches whose
     work counter the last CTA clears) replay to the eager result, bit for bit:
