@@ -399,8 +399,11 @@ SR_API sr_status sr_rope_angle(const sr_config* cfg, int32_t pair, int64_t posit
  * - sr_layer_commit: as sr_cache_commit for every session at once: each window's frames
  *   of k_raw (rotated as above) and v written into its ring slots, its slot table updated,
  *   its n advanced by F.
+ * The packed outputs must not overlap the frame-major inputs (every window reads
+ * rows of the whole frame while others write), nor one another.
  * Validation failures (SR_ERR_INVALID_ARG, SR_ERR_ALIGN, SR_ERR_STATE as for the
- * per-session calls) change nothing.
+ * per-session calls) change nothing. Calls that overlap on the GPU with other calls
+ * of the same sessions race on their rings, as for the per-session calls.
  */
 #define SR_MAX_LAYER_WINDOWS 96
 SR_API sr_status sr_layer_rope_gather(sr_session* const* sessions, const sr_window* windows, int32_t n,
