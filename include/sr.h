@@ -333,7 +333,9 @@ SR_API sr_status sr_rope3d_qk_at(sr_session* s, int64_t first_frame, int32_t n_f
  * finite values: sr_session_init zero-fills it when a frame_counter is given.
  * The host mirror of n (sr_session_frames) does not follow replays; sr_session_restore
  * re-synchronises it before host-state calls are mixed in.
- * Without a frame_counter: SR_ERR_STATE.
+ * The frame-count limit of the host-state calls (2^31 - 1 committed frames, the
+ * int32 slot table) holds here too, but the host cannot see replays: the caller
+ * keeps a replayed session below it. Without a frame_counter: SR_ERR_STATE.
  */
 SR_API sr_status sr_rope3d_qk_dev(sr_session* s, int32_t n_frames, void* q, void* k, void* stream);
 SR_API sr_status sr_chunk_attention_dev(sr_session* s, int32_t step, int32_t n_frames, int32_t hist_frames,
