@@ -334,10 +334,11 @@ def hbm_kernel_times(sessions, shape, reps: int = 16, rounds: int = 7):
 
 def run_e2e(shape, args, dev, sess):
     """Same chunk through the public API with the step's inputs copied in from
-    pinned host memory and both steps' outputs copied back, every step. Uploads
-    and read-backs run on two more streams (the host link is full duplex), over
-    three buffer sets: chunk i+2's inputs go up and chunk i-1's outputs come
-    back while chunk i computes; every chunk still moves all of its own inputs
+    pinned host memory and both steps' outputs copied back, every step, each
+    direction as one copy of a contiguous block. Uploads and read-backs run on
+    two more streams (the host link is full duplex), over three buffer sets:
+    chunk i+2's inputs go up and chunk i-1's outputs come back while chunk i
+    computes; every chunk still moves all of its own inputs
     and outputs inside the timed region, which starts before the first upload
     and ends after the last read-back. Reported: the median of three such
     timed runs of n chunks."""
@@ -346,13 +347,14 @@ def run_e2e(shape, args, dev, sess):
     dims = (shape.lq, shape.n_heads, shape.head_dim)
     g = torch.Generator().manual_seed(1234)
     n_in = 3 * shape.n_steps + 2
-    host_in = [[torch.randn(dims, generator=g).to(torch.bfloat16).pin_memory() for _ in range(n_in)]
-               for _ in range(nbuf)]
-    host_out = [[torch.empty(dims, dtype=torch.bfloat16).pin_memory() for _ in range(shape.n_steps)]
-                for _ in range(nbuf)]
-    dev_in = [[torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in range(n_in)] for _ in range(nbuf)]
-    dev_out = [[torch.empty(dims, dtype=torch.bfloat16, device=dev) for _ in range(shape.n_steps)]
-               for _ in range(nbuf)]
+    # one contiguous block per buffer set and direction, so that a chunk's
+    # inputs go up in one copy and its outputs come back in one copy
+    host_in_blk = [torch.randn((n_in,) + dims, generator=g).to(torch.bfloat16).pin_memory() for _ in range(nbuf)]
+    host_out_blk = [torch.empty((shape.n_steps,) + dims, dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
+    dev_in_blk = [torch.empty((n_in,) + dims, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    dev_out_blk = [torch.empty((shape.n_steps,) + dims, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    dev_in = [list(blk.unbind(0)) for blk in dev_in_blk]
+    dev_out = [list(blk.unbind(0)) for blk in dev_out_blk]
     comp = torch.cuda.current_stream(dev)
     h2d = torch.cuda.Stream(dev)
     d2h = torch.cuda.Stream(dev)
@@ -367,8 +369,7 @@ def run_e2e(shape, args, dev, sess):
             with torch.cuda.stream(h2d):
                 if i >= nbuf:
                     h2d.wait_event(done[i - nbuf])   # buffer set b is free again
-                for h, d in zip(host_in[b], dev_in[b]):
-                    d.copy_(h, non_blocking=True)
+                dev_in_blk[b].copy_(host_in_blk[b], non_blocking=True)
                 up[i].record(h2d)
         for i in range(min(nbuf - 1, chunks)):
             upload(i)
@@ -387,8 +388,7 @@ def run_e2e(shape, args, dev, sess):
             done[i].record(comp)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(done[i])
-                for d, h in zip(dev_out[b], host_out[b]):
-                    h.copy_(d, non_blocking=True)
+                host_out_blk[b].copy_(dev_out_blk[b], non_blocking=True)
                 down[i].record(d2h)
         torch.cuda.synchronize()
 
