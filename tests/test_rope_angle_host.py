@@ -45,7 +45,7 @@ POSITIONS = [0, 1, -1, 7, 44, 79, 1000, 123457, 2 ** 24 - 1, 2 ** 24, 2 ** 24 + 
              -(2 ** 40) - 3, 2 ** 42 - 1, -(2 ** 42) + 1]
 
 
-@pytest.mark.parametrize("head_dim,base", [(128, 10000.0), (64, 500.0), (128, 1.5)])
+@pytest.mark.parametrize("head_dim,base", [(128, 10000.0), (64, 500.0), (128, 1.5), (64, 1.0001), (128, 1.0e6)])
 def test_library_angle_matches_the_exact_reduction(lib, head_dim, base):
     cfg = _cfg(head_dim, base)
     rng = np.random.default_rng(head_dim)
