@@ -168,3 +168,41 @@ def test_random_frame_counts_and_history_windows_match_oracle(case, device_state
     assert_rotated_close(rk[occ], ok_[occ], f"case {case} ring K")
     assert gpu.error_status() == 0
     gpu.close()
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_random_decoder_layers_match_oracle(case):
+    """Random latent grids, window sizes, shifts, chunk lengths and cache depths
+    through a decoder layer's three launches (gather + RoPE, batched attention,
+    commit), against the oracle's whole-frame layer."""
+    from chunked_kv_cache_gb300.decoder import DecoderWindowLayer
+    from oracle.decoder import DecoderLayerOracle
+    rng = np.random.default_rng(4000 + case)
+    dev = device()
+    H, d = int(rng.integers(1, 4)), int(rng.choice([64, 128]))
+    window = int(rng.choice([4, 8, 16]))
+    gh, gw = int(rng.integers(window // 2 + 1, 25)), int(rng.integers(window // 2 + 1, 25))
+    shifted = bool(rng.random() < 0.5)
+    F = int(rng.integers(1, 4))
+    C = int(rng.choice([0, F, 2 * F]))
+    G = int(rng.choice([1, 5]))
+    lay = DecoderWindowLayer(gh, gw, H, d, G, window=window, shifted=shifted, chunk_frames=F, cache_frames=C,
+                             t_clock0=11, device=dev)
+    ora = DecoderLayerOracle(gh, gw, window, shifted, H, d, cache_frames=C, t_clock0=11)
+    idx = lay.packing_index().numpy()
+    bits = lambda b: torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+    for c in range(3):
+        q, k, v, ck, cv = (syn.normal_bf16_bits((F, gh, gw, H, d), rng) for _ in range(5))
+        gk, gv = syn.normal_bf16_bits((G, H, d), rng), syn.normal_bf16_bits((G, H, d), rng)
+        lay.set_global(bits(gk), bits(gv))
+        qp, kp, vp = lay.gather_rope(bits(q), bits(k), bits(v))
+        o = lay.attention(qp, kp, vp)
+        lay.commit(bits(ck), bits(cv))
+        ref = ora.step(q, k, v, gk, gv)
+        ora.commit(ck, cv)
+        got = np.empty((F * gh * gw, H, d))
+        got[idx] = o.float().cpu().numpy()
+        what = f"case {case}: {gh}x{gw} window {window} shifted={shifted} F={F} C={C} H={H} d={d} G={G} chunk {c}"
+        assert_attention_close(got, ref.reshape(-1, H, d), what)
+    assert lay.error_status() == 0
+    lay.close()
