@@ -922,11 +922,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       // the K/V stage that shared mode leaves unused (D = 128), reads them back
       // four rows per instruction and stores them so that every 128-byte row
       // segment is written whole by 8 lanes. No barrier beyond the warp and no
-      // copy engine: a tile store through the tensor-memory-access unit queued
-      // behind the next unit's loads, and its round trips (staging barrier,
-      // store, wait for the read) took 3 us of a 23 us decoder unit. Not when
-      // the next unit is a split-mode one, whose third stage pair lives in that
-      // stage (its record is out long before this).
+      // copy engine (a tile store queues behind the next unit's loads). Not
+      // when the next unit is a split-mode one, whose third stage pair lives in
+      // that stage (its record is usually out long before this).
       bool staged = false;
       if (D == 128 && ok && !wk.split && parts == 1 && r.q_local0 + t * BM < S.lq) {
         const int kn = uk + 1;
