@@ -33,9 +33,13 @@
 //               pairs (a K slot and a V slot behind one barrier), in the
 //               order the MMA consumes them
 //   warps 10-11 idle (they complete the third warpgroup)
-// Registers: launched at 168 per thread (384 x 168 = 64512); the third
-// warpgroup gives back down to 136 and the two softmax warpgroups take 184
-// each: 2 x 128 x 184 + 128 x 136 = 64512, the launch's total.
+//   warps 12-15 epilogue (head dim 128, two-tile units): read O_t out of TMEM
+//               once its last PV MMAs are done, normalise it, stage the rows per
+//               warp in shared memory and store them, while the softmax groups
+//               already work on the next unit
+// Registers: launched at 128 per thread (512 x 128 = 65536); the third and
+// fourth warpgroups give back down to 80 and 64 and the two softmax warpgroups
+// take 184 each: 2 x 128 x 184 + 128 x 80 + 128 x 64 = 65536, the launch's total.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) fp32 scores, O0 [256,256+d)
 // O1 [384,384+d) fp32 accumulators. P (bf16) is written back over the first
 // 64 columns of its S region and fed to the PV MMA straight from TMEM.
@@ -65,10 +69,13 @@ constexpr int BM = 128;      // rows per query tile
 constexpr int BN = 128;      // keys per K/V tile
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
-constexpr int kLaunchRegs = 168;
+constexpr int kEpiWarp0 = 12;   // first warp of the epilogue warpgroup
+constexpr int kLaunchRegs = 128;
 constexpr uint32_t kRegsSoftmax = 184;
-constexpr uint32_t kRegsOther = 136;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kAttnThreads * kLaunchRegs,
+constexpr uint32_t kRegsOther = 80;
+constexpr uint32_t kRegsEpi = 64;
+static_assert(kEpiWarp0 * 32 + 128 == kAttnThreads, "the epilogue warpgroup is the last one");
+static_assert(2 * 128 * kRegsSoftmax + 128 * (kRegsOther + kRegsEpi) <= kAttnThreads * kLaunchRegs,
               "register split exceeds what the block is launched with");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -141,10 +148,16 @@ struct SmemBars {
   uint64_t part_done;     // key split: group 0's partial rows are published
   uint64_t part_last;     // key split: `last` is set
   uint64_t drain;
+  uint64_t il_full[2];    // two-tile unit: softmax group t has published 1/l of its rows
+  uint64_t il_free[2];    // the epilogue warpgroup has read them
+  uint64_t o_free[2];     // the epilogue warpgroup has read O_t: the next PV may overwrite it
   uint32_t tmem_base;
   int abort;
   int last;       // key-split last block: this CTA is the last part and merges
-  float xm[BM];   // split mode: group 1's running max / sum, handed to group 0
+  int stage_done; // epilogue warps done with a unit's staging (4 per two-tile unit)
+  // split mode: group 1's running max / sum, handed to group 0; two-tile unit:
+  // 1/l of tile 0 (xm) and tile 1 (xl), handed to the epilogue warpgroup
+  float xm[BM];
   float xl[BM];
   UnitRec rec[kUnitSlots];
 };
@@ -225,48 +238,6 @@ __device__ __noinline__ void merge_key_parts(const float* __restrict__ hbase, in
   }
 }
 
-// The output rows of one 128-row tile of a shared-mode unit, one 64-column
-// atom at a time through this warp's 4 KB of shared memory (16-byte chunk j of
-// the warp's row rr at rr * 128 + ((j ^ (rr % 8)) * 16), so neither the writes
-// nor the reads conflict on banks): each thread writes its row's atom, then
-// each lane reads chunk lane % 8 of rows lane / 8, lane / 8 + 4, ... and stores
-// it, so that 8 lanes write each 128-byte row segment whole. orow: this lane's
-// first row and chunk in global memory; ostride: four rows; live: the lane's
-// rows 4i + lane / 8 with 4i < live belong to the session. Out of line: it runs
-// once per unit and keeps its registers out of the softmax loop's allocation.
-template <int D>
-__device__ __noinline__ void store_rows_staged(uint32_t t_o, float f0, uint8_t* wbuf, __nv_bfloat16* orow,
-                                               int64_t ostride, int live, int lane) {
-#pragma unroll 1
-  for (int a = 0; a < D / 64; ++a) {
-    __syncwarp();   // the previous atom's reads of the buffer are done
-#pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      uint32_t o[32];
-      tmem_ld32(t_o + (a * 2 + c2) * 32, o);
-      tmem_wait_ld();
-      tmem_fix(o);
-      uint4 pkt[4];
-      uint32_t* w = reinterpret_cast<uint32_t*>(pkt);
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f0, __uint_as_float(o[2 * i + 1]) * f0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(wbuf + lane * 128 + (((c2 * 4 + j) ^ (lane & 7)) * 16)) = pkt[j];
-    }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rr = i * 4 + lane / 8;
-      const uint4 v = *reinterpret_cast<const uint4*>(wbuf + rr * 128 + (((lane % 8) ^ (rr & 7)) * 16));
-      if (4 * i < live) *reinterpret_cast<uint4*>(orow + i * ostride + a * 64) = v;
-    }
-  }
-  __syncwarp();
-  fence_proxy_async_smem();   // the stage may next be filled by a tensor copy
-}
-
 // The key tiles each query tile walks, within the unit's range [lo, lo + n) of
 // all key tiles: in shared mode both walk the whole range; in split mode tile 0
 // walks [lo, lo + h) and tile 1 walks [lo + h, lo + n).
@@ -289,7 +260,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
     // whole blocks, session by session, the blocks of one head next to each
     // other (they read the same keys and values, which then come from L2)
 #pragma unroll 1
-    while (si + 1 < p.n_sess && u >= p.sess[si].unit_begin + H * p.sess[si].nfull) ++si;
+    while (si + 1 < p.n_sess && u >= p.whole_end[si]) ++si;
     const int local = u - p.sess[si].unit_begin;
     const int nf = p.sess[si].nfull;
     head = local / nf;
@@ -300,7 +271,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
     const int b = n_whole + v / 2;
     tile = v % 2;
 #pragma unroll 1
-    while (si + 1 < p.n_sess && b >= p.sess[si].unit_begin + H * p.sess[si].nfull) ++si;
+    while (si + 1 < p.n_sess && b >= p.whole_end[si]) ++si;
     const int local = b - p.sess[si].unit_begin;
     const int nf = p.sess[si].nfull;
     head = local / nf;
@@ -312,7 +283,7 @@ __device__ __forceinline__ void decode_unit(const AttnParams<NSESS>& p, int u, i
     const int tail = t / p.tail_split;
     part = t - tail * p.tail_split;
 #pragma unroll 1
-    while (si + 1 < p.n_sess && tail >= p.sess[si].tail_begin + H * p.sess[si].ntail) ++si;
+    while (si + 1 < p.n_sess && tail >= p.tail_end[si]) ++si;
     head = tail - p.sess[si].tail_begin;
     qb = p.sess[si].nqb - 1;
   }
@@ -440,7 +411,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     mbar_init(&bars->part_done, BM);
     mbar_init(&bars->part_last, 1);
     mbar_init(&bars->drain, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->il_full[t], BM);
+      mbar_init(&bars->il_free[t], BM);
+      mbar_init(&bars->o_free[t], BM);
+    }
     bars->abort = 0;
+    bars->stage_done = 0;
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -459,7 +436,95 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   // bars->rec[k % kUnitSlots] and publishes it on unit_ready (the softmax
   // groups) and q_full (the MMA warp). Every barrier keeps running phase
   // counts across units.
-  if (warp >= 8) {
+  if (warp >= kEpiWarp0) {
+    regs_dec<kRegsEpi>();
+    if constexpr (D == 128) {
+      // ------------------------------------------------------------ epilogue
+      // Two-tile units only (the softmax groups keep the others). Per tile t:
+      // take 1/l of its rows from the softmax group, wait for the last PV MMAs
+      // into O_t, read O_t out of TMEM (scaled, rounded to bf16) into this
+      // warp's 32 rows of the fifth K/V stage, which two-tile units leave
+      // unused, release O_t to the next unit's PV MMAs, then store the rows so
+      // that 16 lanes write each 256-byte row whole. 16-byte chunk j of staged
+      // row rr sits at rr * 256 + ((j & 8) | ((j ^ rr) & 7)) * 16: neither the
+      // row-per-lane writes nor the two-rows-per-instruction reads conflict on
+      // banks.
+      const int eq = warp % 4;   // TMEM lane quarter: rows 32 eq .. 32 eq + 31 of each tile
+      const uint32_t lane_base = static_cast<uint32_t>(eq * 32) << 16;
+      constexpr int kRowBytes = D * 2;
+      uint8_t* stg = sKV + 4 * C::kTileBytes + eq * 32 * kRowBytes;
+      bool ok = true;
+      int uk = 0;
+      uint32_t od0 = 0, od1 = 0;   // o_done completions of each tile so far
+      uint32_t nw = 0;             // two-tile units so far
+      while (ok) {
+        ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[uk % kUnitSlots], (uk / kUnitSlots) & 1, wc, 12));
+        if (!ok) break;
+        const UnitRec& r = bars->rec[uk % kUnitSlots];
+        if (r.u < 0) break;
+        const bool split = r.n_qtiles == 1;
+        const uint32_t w0 = od0, w1 = od1;
+        od0 += 1u;
+        od1 += (!split || r.n_kv - (r.n_kv + 1) / 2 > 0) ? 1u : 0u;   // as the softmax groups count
+        ++uk;
+        if (split) continue;
+        const AttnSession& S = p.sess[r.si];
+        const int head = r.head;
+        const int64_t row0 = static_cast<int64_t>(S.q_row0) + r.q_local0 + eq * 32;
+        const int live0 = S.lq - r.q_local0 - eq * 32;
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = __all_sync(0xffffffffu, wait_bounded(&bars->il_full[t], nw & 1u, wc, 13));
+          if (!ok) break;
+          const float inv = (t == 0 ? bars->xm : bars->xl)[eq * 32 + lane];
+          mbar_arrive(&bars->il_free[t]);
+          ok = __all_sync(0xffffffffu, wait_bounded(&bars->o_done[t], (t == 0 ? w0 : w1) & 1u, wc, 14));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t t_o = tmem + lane_base + 256 + t * 128;
+          uint8_t* mine = stg + lane * kRowBytes;
+#pragma unroll 1
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t o[16];
+            tmem_ld16(t_o + q * 16, o);
+            tmem_wait_ld();
+            tmem_fix(o);
+            uint4 pk[2];
+            uint32_t* w = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int j = 2 * q + h;
+              *reinterpret_cast<uint4*>(mine + ((j & 8) | ((j ^ lane) & 7)) * 16) = pk[h];
+            }
+          }
+          // O_t is read: the next unit's PV MMAs may overwrite it
+          tc_fence_before();
+          mbar_arrive(&bars->o_free[t]);
+          __syncwarp();
+          const int live = live0 - t * BM;
+          const int64_t ld = static_cast<int64_t>(p.n_heads) * D;
+          __nv_bfloat16* orow = p.o + (row0 + t * BM) * ld + head * D;
+#pragma unroll 4
+          for (int i = 0; i < 16; ++i) {
+            const int rr = 2 * i + lane / 16, j = lane % 16;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kRowBytes + ((j & 8) | ((j ^ rr) & 7)) * 16);
+            if (rr < live) *reinterpret_cast<uint4*>(orow + rr * ld + j * 8) = v;
+          }
+          __syncwarp();
+        }
+        ++nw;
+        // the stage may next be filled by a tensor copy (a single-tile unit)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          atomicAdd(&bars->stage_done, 1);
+        }
+      }
+    }
+  } else if (warp >= 8) {
     regs_dec<kRegsOther>();
     if (warp == kTmaWarp && lane == 0) {
       // ---------------------------------------------------------- producer
@@ -472,6 +537,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       int q_last = -1;       // the last unit whose Q load was issued
       int q_shared = 0, q_split = 0;   // pair loads issued so far, per mode
       int mode = -1;         // the previous unit's mode
+      uint32_t nwg = 0;      // two-tile units (head dim 128) issued: their rows are staged in the fifth stage
       auto slot_ptr = [&](int slot) -> uint8_t* {
         return slot < C::kStages ? sKV + slot * C::kTileBytes : sQ + C::kTileBytes;
       };
@@ -516,6 +582,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           const int qm = mode ? q_split : q_shared;
           for (int k = max(0, qm - np); k < qm && ok; ++k)
             ok = wait_bounded(&bars->kv_empty[b0 + k % np], (k / np) & 1, wc, 1);
+          // split mode also loads into the fifth stage, where the epilogue
+          // warpgroup stages output rows: wait until it is done with every
+          // two-tile unit so far (four warps count each)
+          if (ok && md == 1 && D == 128 && nwg > 0) ok = wait_count(&bars->stage_done, static_cast<int>(4 * nwg), wc, 16);
           if (!ok) break;
         }
         mode = md;
@@ -571,6 +641,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           q_split = q;
         else
           q_shared = q;
+        if (D == 128 && !md) ++nwg;
         if (!ok) break;
         u = next_unit(p, tagged);   // taken once this unit's loads are all issued
         publish(uk + 1, u);
@@ -603,6 +674,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       int pc_shared = 0, pc_split = 0;
       uint32_t ph_shared = 0, ph_split = 0;
       uint32_t pb0 = 0, pb1 = 0;   // P tiles of each softmax group waited on so far
+      uint32_t nwg = 0;            // two-tile units whose O the epilogue warpgroup reads out
+      bool prev_wg = false;        // the previous unit was one of them
       // shared-memory address of a K/V stage (the extra split-mode stage is the second Q slot)
       auto stage_addr = [&](int stage) -> uint32_t {
         return stage < C::kStages ? skv + stage * C::kTileBytes : sq + C::kTileBytes;
@@ -655,6 +728,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             mma_ts_w(d_tmem, a_tmem + kk * 8, bd, C::kIdescPV, (acc || kk > 0) ? 1u : 0u, leader);
           }
         };
+        // The epilogue warpgroup has read O_t of the previous unit: the unit's
+        // first PV MMA into O_t may overwrite it.
+        auto free_o = [&](int t) {
+          if (prev_wg && ok) ok = __all_sync(0xffffffffu, wait_bounded(&bars->o_free[t], (nwg - 1) & 1u, wc, 15));
+          tc_fence_after();
+        };
         // O_t += P_t V of iteration it, each part of P as soon as it is stored
         auto pv = [&](int t, int stage, bool acc, int it) {
           wait_p(t, it, true);
@@ -687,8 +766,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           // iterations 1 .. n-1: PV_{i-1} and S_i of both tiles from one pair
           // (K_i, V_{i-1}). Its wait comes first, while the warp would otherwise
           // be waiting for softmax group 0; between S0_i and PV1_{i-1} there is
-          // only that group's wait.
-          for (int i = 1; i < n && ok; ++i) {
+          // only that group's wait. Iteration 1 holds the unit's first PV of
+          // each tile, which may have to wait until O_t is read out: peeled.
+          if (n > 1 && ok) {
+            const int pi = take();
+            tc_fence_after();
+            free_o(0);
+            pv(0, 2 * pi + 1, false, 0);
+            if (ok) {
+              qk(0, 2 * pi);
+              tc_commit_w(&bars->s_full[0], leader);
+              free_o(1);
+              pv(1, 2 * pi + 1, false, 0);
+            }
+            if (ok) {
+              qk(1, 2 * pi);
+              tc_commit_w(&bars->s_full[1], leader);
+              tc_commit_w(&bars->kv_empty[bar0 + pi], leader);
+            }
+          }
+          for (int i = 2; i < n && ok; ++i) {
             const int pi = take();
             tc_fence_after();
             pv(0, 2 * pi + 1, i > 1, i - 1);
@@ -707,10 +804,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           if (ok) {
             const int pl = take();
             tc_fence_after();
+            if (ok && n == 1) free_o(0);
             if (ok) pv(0, 2 * pl + 1, n > 1, n - 1);
             if (ok) {
               tc_commit_w(&bars->o_done[0], leader);
-              pv(1, 2 * pl + 1, n > 1, n - 1);
+              if (n == 1) free_o(1);
+              if (ok) pv(1, 2 * pl + 1, n > 1, n - 1);
             }
             if (ok) {
               tc_commit_w(&bars->o_done[1], leader);
@@ -723,6 +822,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           // t, one pair holding K(t, i) and V(t, i-1); tile 1's wait comes after
           // tile 0's MMAs are queued.
           const int c0 = wk.count(0), c1 = wk.count(1);
+          free_o(0);
+          free_o(1);
           for (int i = 0; i <= c0 && ok; ++i) {
             const bool p0 = i > 0 && i - 1 < c0, q0 = i < c0;
             if (p0 || q0) {
@@ -770,6 +871,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         }
         pb0 += static_cast<uint32_t>(wk.count(0));
         pb1 += static_cast<uint32_t>(wk.count(1));
+        prev_wg = D == 128 && !wk.split;
+        if (prev_wg) ++nwg;
         ++uk;
       }
       if (!ok && issued_any) {
@@ -794,6 +897,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     uint32_t od0 = 0, od1 = 0;   // o_done completions of each tile so far
     uint32_t nx = 0;             // split-mode units so far
     uint32_t nk = 0;             // key-split units so far
+    uint32_t nwg = 0;            // two-tile units handed to the epilogue warpgroup
+    uint32_t nwg_seen = 0;       // of those, known to be finished by it
     while (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[uk % kUnitSlots], (uk / kUnitSlots) & 1, wc, 8));
       if (!ok) break;
@@ -892,6 +997,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       }
       sb += static_cast<uint32_t>(cnt);
 
+      if (D == 128 && !wk.split) {
+        // Two-tile unit: the epilogue warpgroup normalises and stores O_t. Hand
+        // it 1/l of this group's rows (once it has read the previous unit's),
+        // write the LSE here and go on to the next unit.
+        const int q_local = r.q_local0 + t * BM + row;
+        if (ok && p.lse != nullptr && q_local < S.lq)
+          p.lse[static_cast<int64_t>(head) * p.lse_ld + S.q_row0 + q_local] = (m + __log2f(l)) * 0.69314718055994531f;
+        if (ok && nwg > 0) ok = __all_sync(0xffffffffu, wait_bounded(&bars->il_free[t], (nwg - 1) & 1u, wc, 17));
+        (t == 0 ? bars->xm : bars->xl)[row] = 1.f / l;
+        mbar_arrive(&bars->il_full[t]);
+        ++nwg;
+        od0 += 1u;
+        od1 += 1u;
+        ++uk;
+        continue;
+      }
+
       // ---- epilogue: normalise and store (in split mode group 0 merges both halves)
       const int q_local = r.q_local0 + (wk.split ? 0 : t) * BM + row;
       const bool live = q_local < S.lq;
@@ -902,7 +1024,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       od1 += (!wk.split || wk.count(1) > 0) ? 1u : 0u;
       if (wk.split && t == 1) {
         // hand (m, l) to group 0, then wait until it has read them and O_1:
-        // this group's next P (and so the next PV into O_1) comes only after
+        // this group's next P (and so the next PV into O_1) comes only after.
+        // xm / xl last carried 1/l to the epilogue warpgroup, which must be
+        // done with every two-tile unit so far (four warps count each).
+        if (D == 128 && ok && nwg > nwg_seen) {
+          ok = __all_sync(0xffffffffu, wait_count(&bars->stage_done, static_cast<int>(4 * nwg), wc, 18));
+          nwg_seen = nwg;
+        }
         bars->xm[row] = (ok && cnt > 0) ? m : -INFINITY;
         bars->xl[row] = (ok && cnt > 0) ? l : 0.f;
         mbar_arrive(&bars->x_full);
@@ -916,21 +1044,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         ok = wait_bounded(&bars->o_done[t], (t == 0 ? w0 : w1) & 1u, wc, 6);
         if (ok && merge) ok = wait_bounded(&bars->o_done[1], w1 & 1u, wc, 6);
         ok = __all_sync(0xffffffffu, ok);
-      }
-      // The output rows of a shared-mode unit leave through shared memory, one
-      // 64-column atom at a time: each warp writes its 32 rows into its 4 KB of
-      // the K/V stage that shared mode leaves unused (D = 128), reads them back
-      // four rows per instruction and stores them so that every 128-byte row
-      // segment is written whole by 8 lanes. No barrier beyond the warp and no
-      // copy engine (a tile store queues behind the next unit's loads). Not
-      // when the next unit is a split-mode one, whose third stage pair lives in
-      // that stage (its record is usually out long before this).
-      bool staged = false;
-      if (D == 128 && ok && !wk.split && parts == 1 && r.q_local0 + t * BM < S.lq) {
-        const int kn = uk + 1;
-        ok = __all_sync(0xffffffffu, wait_bounded(&bars->unit_ready[kn % kUnitSlots], (kn / kUnitSlots) & 1, wc, 11));
-        const UnitRec& rn = bars->rec[kn % kUnitSlots];
-        staged = ok && (rn.u < 0 || rn.n_qtiles == 2);
       }
       // one part of a key-split last block publishes fp32 rows and their log2-sum-exp
       float* pdst = parts > 1 ? S.ws_part + ((static_cast<int64_t>(head) * kMaxTailSplit + part) * BM + row) * (D + 4)
@@ -951,16 +1064,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         f1 *= inv_l;
         __nv_bfloat16* dst = p.o + (out_row * p.n_heads + head) * D;
         const uint32_t t_o1 = tmem + lane_base + 256 + 128;
-        if (staged) {
-          const int live = S.lq - (r.q_local0 + t * BM) - (warp % 4) * 32 - lane / 8;
-          const int64_t grow = static_cast<int64_t>(S.q_row0) + r.q_local0 + t * BM + (warp % 4) * 32 + lane / 8;
-          store_rows_staged<D>(t_o, f0, sKV + 4 * C::kTileBytes + t * C::kAtomBytes + (warp % 4) * 32 * 128,
-                               p.o + (grow * p.n_heads + head) * D + (lane % 8) * 8,
-                               static_cast<int64_t>(4) * p.n_heads * D, live, lane);
-        }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          if (staged) break;
           uint32_t o[32];
           tmem_ld32(t_o + c * 32, o);
           tmem_wait_ld();

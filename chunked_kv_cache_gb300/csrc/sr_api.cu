@@ -222,10 +222,20 @@ void place_units(sr::AttnSession& g, int n_heads, int& full, int& tails) {
   tails += n_heads * g.ntail;
 }
 
+// The packed unit ranges of the launch's query groups (after place_units).
+template <int N>
+void index_units(sr::AttnParams<N>& p) {
+  for (int i = 0; i < p.n_sess; ++i) {
+    p.whole_end[i] = p.sess[i].unit_begin + p.n_heads * p.sess[i].nfull;
+    p.tail_end[i] = p.sess[i].tail_begin + p.n_heads * p.sess[i].ntail;
+  }
+}
+
 // The launch's unit count, and the unit counter of a persistent launch: it
 // lives at the start of the first group's workspace (none: one unit per CTA).
 template <int N>
 void set_units(sr::AttnParams<N>& p, int n_units, const sr_session* first) {
+  index_units(p);
   p.n_units = n_units;
   if (first->buf.workspace != nullptr && p.sess[0].ws_ctr != nullptr) {
     p.unit_ctr = static_cast<unsigned long long*>(first->buf.workspace);
@@ -901,6 +911,7 @@ sr_status sr_window_attention(sr_session* s, int32_t step, int32_t moving_frames
     }
     p->n_conv = conv;
     p->n_units = full + conv + tails;
+    index_units(*p);
     if (s->buf.workspace) {
       p->unit_ctr = static_cast<unsigned long long*>(s->buf.workspace);
       p->epoch = next_epoch(s);

@@ -94,6 +94,23 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
   return wait_bounded_slow(bar, parity, w, site);
 }
 
+// Bounded wait until a shared-memory counter reaches `target` (the CTA aborts
+// on a time-out, like wait_bounded). The fence after it orders this thread's
+// later accesses behind the counted work.
+__device__ __forceinline__ bool wait_count(const volatile int* ctr, int target, const WaitCtx& w, int site) {
+  const uint64_t t0 = globaltimer_ns();
+  while (*ctr < target) {
+    if (*w.abort) return false;
+    if (globaltimer_ns() - t0 > w.timeout_ns) {
+      raise_error(w, site);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence_block();
+  return true;
+}
+
 // Used only while tearing down after an abort: waits for this CTA's own
 // copies / MMAs in flight, ignoring the abort flag, again with a time limit.
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -235,10 +252,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : SR_R8(0), SR_R8(8), SR_R8(16), SR_R8(24)
       : "r"(taddr));
 }
+// 32 lanes x 16 consecutive 32-bit columns (same lane mapping as tmem_ld32).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : SR_R8(0), SR_R8(8)
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_fix(uint32_t (&r)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+__device__ __forceinline__ void tmem_fix(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(

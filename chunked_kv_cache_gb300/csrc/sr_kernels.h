@@ -80,6 +80,12 @@ template <int NSESS>
 struct alignas(128) AttnParams {
   CUtensorMap qmap;               // packed q, [total_rows][H*d]
   AttnSession sess[NSESS];
+  // Unit ranges of the sessions, packed so that finding a unit's session reads
+  // a few contiguous words rather than one field of each (large) session:
+  // whole-block units of session i end at whole_end[i], its last-block units
+  // (among all last-block units) at tail_end[i].
+  int32_t whole_end[NSESS];
+  int32_t tail_end[NSESS];
   int32_t n_sess;
   int32_t n_full_units;           // whole 256-row blocks (all sessions); last blocks follow
   int32_t n_conv;                 // the last n_conv whole blocks each run as two single-tile units,
@@ -99,7 +105,7 @@ struct alignas(128) AttnParams {
   unsigned long long* unit_ctr;
 };
 
-constexpr int kAttnThreads = 384;  // 2 softmax warpgroups, then MMA warp, TMA warp and 2 idle warps
+constexpr int kAttnThreads = 512;  // 2 softmax warpgroups; MMA warp, TMA warp, 2 idle warps; the epilogue warpgroup
 constexpr int kAttnMaxBatch = SR_MAX_BATCH;
 
 int attn_smem_bytes(int head_dim);
