@@ -107,6 +107,8 @@ struct alignas(128) AttnParams {
 
 constexpr int kAttnThreads = 512;  // 2 softmax warpgroups; MMA warp, TMA warp, 2 idle warps; the epilogue warpgroup
 constexpr int kAttnMaxBatch = SR_MAX_BATCH;
+// A kernel's parameters may take at most 32764 bytes.
+static_assert(sizeof(AttnParams<kAttnMaxBatch>) <= 32764, "attention parameters exceed the kernel parameter limit");
 
 int attn_smem_bytes(int head_dim);
 cudaError_t attn_prepare(int head_dim, int nsess_template);   // sets the smem attribute
