@@ -128,6 +128,7 @@ struct UnitRec {
   int u;                 // unit index; -1 once the CTA has no more work
   int si, head, part, parts;
   int q_local0;          // first query row of the unit (session-local)
+  int q_row0, lq;        // the session's first row in the packed q / o, and its query rows
   int n_qtiles;          // 2 (shared mode) or 1 (split mode)
   int kv_lo, n_kv;       // the unit's range of the session's key tiles
   TileMap tm;
@@ -334,6 +335,8 @@ __device__ __forceinline__ void make_unit(const AttnParams<NSESS>& p, int u, Uni
   r.part = part;
   r.q_local0 = qb * 2 * BM + (tile > 0 ? BM : 0);
   r.n_qtiles = tile >= 0 ? 1 : min(2, (S.lq - r.q_local0 + BM - 1) / BM);
+  r.q_row0 = S.q_row0;
+  r.lq = S.lq;
   // a single-tile last block may be one of `parts` units sharing its key range
   r.parts = (tile < 0 && r.n_qtiles == 1 && S.ws_part != nullptr) ? p.tail_split : 1;
   r.kv_lo = static_cast<int>(static_cast<int64_t>(part) * n_kv_all / r.parts);
@@ -468,10 +471,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         od1 += (!split || r.n_kv - (r.n_kv + 1) / 2 > 0) ? 1u : 0u;   // as the softmax groups count
         ++uk;
         if (split) continue;
-        const AttnSession& S = p.sess[r.si];
         const int head = r.head;
-        const int64_t row0 = static_cast<int64_t>(S.q_row0) + r.q_local0 + eq * 32;
-        const int live0 = S.lq - r.q_local0 - eq * 32;
+        const int64_t row0 = static_cast<int64_t>(r.q_row0) + r.q_local0 + eq * 32;
+        const int live0 = r.lq - r.q_local0 - eq * 32;
         for (int t = 0; t < 2 && ok; ++t) {
           ok = __all_sync(0xffffffffu, wait_bounded(&bars->il_full[t], nw & 1u, wc, 13));
           if (!ok) break;
@@ -598,7 +600,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         for (int t = 0; t < r.n_qtiles; ++t)
           for (int a = 0; a < C::kAtoms; ++a)
             tma_load_2d(sQ + t * C::kTileBytes + a * C::kAtomBytes, &p.qmap, &bars->q_full,
-                        r.head * D + a * 64, S.q_row0 + r.q_local0 + t * BM, pol_q);
+                        r.head * D + a * 64, r.q_row0 + r.q_local0 + t * BM, pol_q);
         q_last = uk;
         const int npair = md ? C::kPairsSplit : C::kPairs;
         const int bar0 = md ? 4 : 0;
@@ -1002,8 +1004,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         // it 1/l of this group's rows (once it has read the previous unit's),
         // write the LSE here and go on to the next unit.
         const int q_local = r.q_local0 + t * BM + row;
-        if (ok && p.lse != nullptr && q_local < S.lq)
-          p.lse[static_cast<int64_t>(head) * p.lse_ld + S.q_row0 + q_local] = (m + __log2f(l)) * 0.69314718055994531f;
+        if (ok && p.lse != nullptr && q_local < r.lq)
+          p.lse[static_cast<int64_t>(head) * p.lse_ld + r.q_row0 + q_local] = (m + __log2f(l)) * 0.69314718055994531f;
         if (ok && nwg > 0) ok = __all_sync(0xffffffffu, wait_bounded(&bars->il_free[t], (nwg - 1) & 1u, wc, 17));
         (t == 0 ? bars->xm : bars->xl)[row] = 1.f / l;
         mbar_arrive(&bars->il_full[t]);
@@ -1016,8 +1018,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 
       // ---- epilogue: normalise and store (in split mode group 0 merges both halves)
       const int q_local = r.q_local0 + (wk.split ? 0 : t) * BM + row;
-      const bool live = q_local < S.lq;
-      const int64_t out_row = static_cast<int64_t>(S.q_row0) + q_local;
+      const bool live = q_local < r.lq;
+      const int64_t out_row = static_cast<int64_t>(r.q_row0) + q_local;
       const bool merge = wk.split && wk.count(1) > 0;
       const uint32_t w0 = od0, w1 = od1;   // this unit's o_done phases
       od0 += 1u;
