@@ -437,8 +437,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   // CTA per SM) then takes further units from the launch-wide counter. Each
   // role walks the same sequence of units: the producer decodes a unit into
   // bars->rec[k % kUnitSlots] and publishes it on unit_ready (the softmax
-  // groups) and q_full (the MMA warp). Every barrier keeps running phase
-  // counts across units.
+  // groups and the epilogue warpgroup) and q_full (the MMA warp). A slot is
+  // reused four units later: by then the MMA warp has waited for the epilogue
+  // warpgroup to read out at least unit k - 3, after it read that record.
+  // Every barrier keeps running phase counts across units.
   if (warp >= kEpiWarp0) {
     regs_dec<kRegsEpi>();
     if constexpr (D == 128) {
