@@ -40,7 +40,11 @@ def assert_rotated_close(gpu_bits, ref_bits, what=""):
     rounded value, plus the fp32 evaluation error of the rotation, which is
     absolute (bounded by 2^-19 times the pair's norm) and so exceeds an ulp
     only for outputs that nearly cancel. Almost every element must match
-    bit for bit."""
+    bit for bit: all but 0.1 %, or all but two in a tensor of fewer than
+    2000 elements. An element whose exact value lies within the fp32
+    evaluation error of a bf16 rounding midpoint may round to the other
+    neighbour, a few in 10^5 of them; in a 256-element tensor one such flip
+    is 0.4 %."""
     g = bf16_bits_to_f64(np.asarray(gpu_bits))
     r = bf16_bits_to_f64(np.asarray(ref_bits))
     pair = np.sqrt(r[..., 0::2] ** 2 + r[..., 1::2] ** 2)
@@ -52,8 +56,9 @@ def assert_rotated_close(gpu_bits, ref_bits, what=""):
     worst = np.argmax(err - bound)
     assert np.all(err <= bound), (f"{what}: |gpu-ref| {err.flat[worst]:.3e} > bound {bound.flat[worst]:.3e} "
                                   f"(ref {r.flat[worst]:.4e}, gpu {g.flat[worst]:.4e})")
-    frac = (np.asarray(gpu_bits) != np.asarray(ref_bits)).mean()
-    assert frac < 1e-3, f"{what}: {frac:.2e} of elements not bit-identical"
+    n_diff = int((np.asarray(gpu_bits) != np.asarray(ref_bits)).sum())
+    n = np.asarray(gpu_bits).size
+    assert n_diff <= max(1e-3 * n, 2), f"{what}: {n_diff} of {n} elements not bit-identical"
 
 
 def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
