@@ -40,7 +40,7 @@ def _draw_shape(rng, case):
     return syn.Shape(f"fuzz {case}", H, d, gh, gw, F, W, S, steps)
 
 
-@pytest.mark.parametrize("case", range(48))
+@pytest.mark.parametrize("case", range(96))
 def test_random_session_shapes_match_oracle(case):
     rng = np.random.default_rng(1000 + case)
     shape = _draw_shape(rng, case)
@@ -76,7 +76,7 @@ def test_random_session_shapes_match_oracle(case):
     assert tw.gpu.error_status() == 0
 
 
-@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("case", range(24))
 def test_random_batches_match_single_calls_and_oracle(case):
     import chunked_kv_cache_gb300 as sr
     rng = np.random.default_rng(2000 + case)
@@ -111,7 +111,7 @@ def test_random_batches_match_single_calls_and_oracle(case):
         assert tw.gpu.error_status() == 0
 
 
-@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("case", range(24))
 @pytest.mark.parametrize("device_state", [False, True])
 def test_random_frame_counts_and_history_windows_match_oracle(case, device_state):
     """Chunks of 1 to 5 frames with random visible-history windows through the
@@ -170,7 +170,7 @@ def test_random_frame_counts_and_history_windows_match_oracle(case, device_state
     gpu.close()
 
 
-@pytest.mark.parametrize("case", range(10))
+@pytest.mark.parametrize("case", range(30))
 def test_random_decoder_layers_match_oracle(case):
     """Random latent grids, window sizes, shifts, chunk lengths and cache depths
     through a decoder layer's three launches (gather + RoPE, batched attention,
