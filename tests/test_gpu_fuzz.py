@@ -206,3 +206,40 @@ def test_random_decoder_layers_match_oracle(case):
         assert_attention_close(got, ref.reshape(-1, H, d), what)
     assert lay.error_status() == 0
     lay.close()
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_random_page_faithful_windows_match_oracle(case):
+    """The page-faithful window on random shapes: prefix rows over the bank of
+    the step alone and moving rows (1 to 5 frames) over the bank and
+    themselves, in one launch, with and without a workspace (persistent or one
+    unit per CTA), against the oracle's window_attention."""
+    import chunked_kv_cache_gb300 as sr
+    from oracle import OracleSession
+    rng = np.random.default_rng(5000 + case)
+    d = int(rng.choice([64, 128]))
+    H = int(rng.integers(1, 5))
+    gh, gw = int(rng.integers(1, 13)), int(rng.integers(1, 17))
+    S = int(rng.choice([1, 37, 128, 200, 300]))
+    steps = int(rng.integers(1, 3))
+    sh = syn.Shape(f"window fuzz {case}", H, d, gh, gw, 3, 3, S, steps)
+    moving = int(rng.integers(1, 6))
+    with_prefix = bool(rng.random() < 0.6)
+    workspace = bool(rng.random() < 0.7)
+    dev = device()
+    sk, sv = syn.session_sinks(sh, 11 + case)
+    gpu = sr.Session(H, d, gh, gw, sh.chunk_frames, sh.window_frames, S, steps, sink_k=to_dev(sk, dev),
+                     sink_v=to_dev(sv, dev), t_clock0=5, workspace=workspace, device=dev)
+    ora = OracleSession(H, d, gh, gw, sh.chunk_frames, sh.window_frames, S, steps, sk, sv, t_clock0=5)
+    T = gh * gw
+    P = S if with_prefix else 0
+    for step in range(steps):
+        q, km, vm = (syn.normal_bf16_bits((rows, H, d), rng) for rows in (P + moving * T, moving * T, moving * T))
+        o, lse = gpu.window_attention(step, to_dev(q, dev), to_dev(km, dev), to_dev(vm, dev), moving,
+                                      with_prefix=with_prefix, lse=True)
+        ref, ref_lse = ora.window_attention(step, q, km, vm, with_prefix)
+        assert_attention_close(o.float().cpu().numpy().astype(np.float64), ref,
+                               f"{sh.name} step {step} prefix {with_prefix} moving {moving}")
+        assert np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max() <= LSE_ABS
+    assert gpu.error_status() == 0
+    gpu.close()
