@@ -11,8 +11,10 @@ forced on (so the built-in scratch is really used, and reused by the second
 call): the output against the float64 oracle within the attention tolerances
 of the parity tests, and bit for bit against sr_chunk_attention on a twin
 session that has its own workspace and the same forced split (the same plan,
-so the same arithmetic). A session too large for the scratch is refused before
-anything runs. This file is collected last on purpose.
+so the same arithmetic); and the same two checks on twelve random session
+shapes with forced splits of 1, 2 or 4 parts. A session too large for the
+scratch is refused before anything runs. This file is collected last on
+purpose.
 """
 import numpy as np
 import pytest
@@ -89,3 +91,45 @@ def test_noalloc_refuses_sessions_beyond_its_scratch():
                                      torch.cuda.current_stream(dev).cuda_stream)
     assert e.value.status == N.SR_ERR_UNSUPPORTED
     s.close()
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_noalloc_random_shapes_match_oracle_and_workspace_twin(case):
+    """Random session shapes (1-4 heads of 64 or 128, small grids, 1-3 chunk
+    frames, rings of 0 to 2F+1 frames partly filled, 0-200 sink tokens) with a
+    forced key split of 1, 2 or 4 parts: the allocation-free call against the
+    oracle, and bit for bit against sr_chunk_attention on a twin session with a
+    workspace of its own and the same split."""
+    from chunked_kv_cache_gb300 import _native as N
+    rng = np.random.default_rng(6000 + case)
+    d = int(rng.choice([64, 128]))
+    H = int(rng.integers(1, 5))
+    gh, gw = int(rng.integers(1, 13)), int(rng.integers(1, 17))
+    F = int(rng.integers(1, 4))
+    W = int(rng.choice([0, F, F + 1, 2 * F + 1]))
+    S = int(rng.choice([0, 1, 37, 128, 200]))
+    shape = syn.Shape(f"noalloc fuzz {case}", H, d, gh, gw, F, W, S, 1)
+    fill = int(rng.integers(0, W + 1)) if W else 0
+    split = int(rng.choice([1, 2, 4]))
+    tw = Twin(shape, 7, fill=fill, session=case, tail_split=split, workspace=False)
+    twin = Twin(shape, 7, fill=fill, session=case, tail_split=split, workspace=True)
+    dev = tw.dev
+    x = syn.chunk_inputs(shape, 7, session=case, chunk=1)
+    q, k, v = (to_dev(b, dev) for b in (x.q[0], x.k[0], x.v[0]))
+    tw.gpu.rope3d_qk(q, k)
+    qo, ko = tw.ora.rope3d_qk(x.q[0], x.k[0])
+    ref, ref_lse = tw.ora.chunk_attention(0, qo, ko, x.v[0])
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    same_o = torch.empty_like(q)
+    same_l = torch.empty((H, shape.lq), dtype=torch.float32, device=dev)
+    N.sr_chunk_attention(twin.gpu.handle, 0, q.data_ptr(), k.data_ptr(), v.data_ptr(), same_o.data_ptr(),
+                         same_l.data_ptr(), stream)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((H, shape.lq), float("nan"), dtype=torch.float32, device=dev)
+    N.sr_chunk_attention_noalloc(tw.gpu.handle, 0, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), stream)
+    torch.cuda.synchronize()
+    assert_attention_close(o.float().cpu().numpy().astype(np.float64), ref, f"{shape.name} against the oracle")
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max() <= LSE_ABS
+    assert torch.equal(o, same_o) and torch.equal(lse, same_l), f"{shape.name}: differs from the workspace twin"
+    assert tw.gpu.error_status() == 0 and twin.gpu.error_status() == 0
